@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Benchmark of the fused exact-attention hot path on one GB300 (or N replicas).
+
+One step = one forward (attn_fwd) and one backward (attn_bwd_preprocess,
+attn_bwd_main, attn_bwd_dq_convert: exactly attn_bwd) over the workload's
+batch, inputs resident in HBM.  The default workload is B=4, H=16, N=4096,
+d=128, causal, bf16, the shape the metric's percentage-of-peak target is
+quoted on.  Printed: one JSON line with TFLOP/s of the whole step (FLOPs:
+4 B H N^2 d halved for causal forward, 2.5x that for the backward), the
+per-pass figures, the dominant kernel's roofline, the end-to-end figure
+through the public API with host buffers, the float64 oracle timed on the
+host cores, and the SM clocks sampled during the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_attention_58_gb300.workloads import Workload, make_workload_inputs, workload  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s and % of GB300 dense bf16 tensor peak"
+DEFAULT_WORKLOAD = 3
+FALLBACK_PEAK_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2**20
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------
+def fwd_compulsory_bytes(w: Workload) -> int:
+    """Q, K, V read and O written once, plus one fp32 LSE per row."""
+    es = 2 if w.dtype == "bf16" else 4
+    return w.B * w.H * (4 * w.N * w.d * es + w.N * 4)
+
+
+def bwd_compulsory_bytes(w: Workload) -> int:
+    """Q, K, V, O, dO read and dQ, dK, dV written once, plus LSE read."""
+    es = 2 if w.dtype == "bf16" else 4
+    return w.B * w.H * (8 * w.N * w.d * es + w.N * 4)
+
+
+def valid_pairs_in_rows(w: Workload, row0: int, nrows: int) -> int:
+    """(query, key) pairs a slice of query rows attends to (no key padding)."""
+    if not w.causal:
+        return nrows * w.N
+    return sum(i + 1 for i in range(row0, row0 + nrows))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk["bf16_tflops_sustained"]), float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_PEAK_TFLOPS, 1700.0, FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("attn_fwd.cu", "attn_bwd.cu", "ptx.cuh", "philox.cuh"):
+        with open(os.path.join(ROOT, "exact_attention_58_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        e = rec[kernel][workload_name]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import torch
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.device_index).uuid)
+        except Exception:
+            uuid = str(self.device_index)
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={uuid}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.4)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the float64 oracle on the host cores (a bounded sample of the same workload)
+# ---------------------------------------------------------------------------
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(inp, w: Workload, heads: int, row0: int, nrows: int, threads: int):
+    """Run the oracle's forward+backward on `nrows` query rows of `heads` heads.
+    Returns (seconds, algorithmic FLOPs of the sample)."""
+    import numpy as np
+
+    import oracle
+    hs = [(x // w.H, x % w.H) for x in range(heads)]
+    sel = lambda t: np.stack([t[b, h].double().numpy() for b, h in hs])  # noqa: E731
+    Q, K, V, dO = sel(inp.q), sel(inp.k), sel(inp.v), sel(inp.do)
+    b_idx = [b for b, _ in hs]
+    h_idx = [h for _, h in hs]
+    kl = [w.N] * heads
+    t0 = time.perf_counter()
+    oracle.heads_rows_fwd_bwd(Q, K, V, dO, b_idx, h_idx, kl, inp.scale, row0, nrows, w.causal,
+                              inp.dropout_p, inp.seed, nthreads=threads)
+    dt = time.perf_counter() - t0
+    flops = heads * valid_pairs_in_rows(w, row0, nrows) * 14.0 * w.d   # 4d fwd + 10d bwd
+    return dt, flops
+
+
+def calibrate_rows(inp, w, heads, threads, target_s):
+    """Rows per head so that one oracle sample takes about target_s seconds."""
+    row0 = w.N // 2
+    oracle_sample(inp, w, heads, row0, 4, threads)           # warm: threads, pages
+    probe = 32
+    dt, _ = oracle_sample(inp, w, heads, row0, probe, threads)
+    per_row = max(dt / probe, 1e-5)
+    return max(1, min(w.N - row0, int(target_s / per_row)))
+
+
+def cpu_baseline(inp, w, target_s=15.0):
+    threads = host_cores()
+    heads = min(threads, w.B * w.H)
+    rows = calibrate_rows(inp, w, heads, threads, target_s)
+    row0 = max(0, w.N // 2 - rows // 2)
+    dt, flops = oracle_sample(inp, w, heads, row0, rows, threads)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"float64 oracle forward+backward of query rows [{row0}, {row0 + rows}) "
+                      f"of {heads} heads of {w.name}, one head per core, {dt:.1f} s; FLOPs "
+                      f"counted as 14 d per attended (query, key) pair"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle, as it stands, on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args, w: Workload):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp = make_workload_inputs(args.workload)
+    threads = host_cores()
+    heads = min(threads, w.B * w.H)
+    per_step = max(0.5, args.reference_budget_s / (args.steps + args.warmup))
+    rows = calibrate_rows(inp, w, heads, threads, per_step)
+    row0 = max(0, w.N // 2 - rows // 2)
+    for _ in range(args.warmup):
+        oracle_sample(inp, w, heads, row0, rows, threads)
+    tot_t, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, fl = oracle_sample(inp, w, heads, row0, rows, threads)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    sample = (f"each step: float64 oracle forward+backward of query rows [{row0}, {row0 + rows}) "
+              f"of {heads} heads of {w.name}, one head per core")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "causal": w.causal, "passes": "fwd+bwd"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "kind": "oracle",
+                             "cores": threads, "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, w: Workload):
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_58_gb300 as ea
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    ea.library()
+
+    inp = make_workload_inputs(args.workload)
+    q, k, v, do = (t.to(dev) for t in (inp.q, inp.k, inp.v, inp.do))
+    kl = inp.key_lens.to(dev) if inp.key_lens is not None else None
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(ea.attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kw = dict(causal=w.causal, key_lens=kl, dropout_p=inp.dropout_p, seed=inp.seed,
+              scale=inp.scale)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record()
+        ea.attn_fwd(q, k, v, out=o, lse=lse, dev_status=status, **kw)
+        if evs:
+            evs[1].record()
+        ea.attn_bwd_preprocess(o, do, lse, ws)
+        if evs:
+            evs[2].record()
+        ea.attn_bwd_main(q, k, v, do, dk, dv, ws, dev_status=status, **kw)
+        if evs:
+            evs[3].record()
+        ea.attn_bwd_dq_convert(dq, ws, scale=inp.scale)
+        if evs:
+            evs[4].record()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    start.record()
+    for s in range(args.steps):
+        step(evs[s])
+    end.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the timed region")
+
+    elapsed_ms = start.elapsed_time(end)
+    per = [[evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps)] for i in range(4)]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    flops_fwd, flops_bwd = w.flops_fwd(), w.flops_bwd()
+    flops_step = flops_fwd + flops_bwd
+    value = world * flops_step * args.steps / (elapsed_ms * 1e-3) / 1e12
+    fwd_ms, pre_ms, main_ms, conv_ms = (statistics.mean(x) for x in per)
+    peak, peak_sus, hbm, peak_src = load_peaks()
+    fwd_tf = flops_fwd / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = flops_bwd / ((pre_ms + main_ms + conv_ms) * 1e-3) / 1e12
+    main_tf = flops_bwd / (main_ms * 1e-3) / 1e12
+    if main_ms >= fwd_ms:
+        dom, dom_tf, dom_ms = "attn_bwd_kernel", main_tf, main_ms
+    else:
+        dom, dom_tf, dom_ms = "attn_fwd_kernel", fwd_tf, fwd_ms
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": dom_tf, "peak": peak,
+                "unit": "TFLOP/s", "frac": dom_tf / peak, "traffic": recorded_traffic(dom, w.name),
+                "peak_source": f"{peak_src} bf16 dense (burst)"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    # ---- end to end through the public API with pinned host buffers ----
+    e2e = None
+    if args.e2e_steps > 0:
+        hq, hk, hv, hdo = (t.pin_memory() for t in (inp.q, inp.k, inp.v, inp.do))
+        ho, hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(4))
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            do.copy_(hdo, non_blocking=True)
+            ea.attn_fwd(q, k, v, out=o, lse=lse, **kw)
+            ea.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
+            ho.copy_(o, non_blocking=True)
+            hdq.copy_(dq, non_blocking=True)
+            hdk.copy_(dk, non_blocking=True)
+            hdv.copy_(dv, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        s_ev.record()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e_ev.record()
+        torch.cuda.synchronize()
+        e_ms = s_ev.elapsed_time(e_ev)
+        nbytes = q.numel() * q.element_size()
+        e2e = {"value": flops_step * args.e2e_steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 4 * nbytes,
+               "ms_per_step": e_ms / args.e2e_steps}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, w, target_s=args.cpu_seconds)
+
+    in_bytes = 4 * q.numel() * q.element_size()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "dropout_p": w.dropout_p, "passes": "fwd+bwd",
+                   "global_batch": world * w.B, "seq_len": w.N,
+                   "parallelism": f"replicas x{world} (heads independent)",
+                   "l2": f"inputs {in_bytes / 2**20:.0f} MiB > L2 {L2_BYTES / 2**20:.0f} MiB, no flush"},
+        "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "fwd_frac_peak": fwd_tf / peak,
+        "bwd_frac_peak": bwd_tf / peak, "peak_tflops": peak,
+        "kernel_ms": {"attn_fwd_kernel": fwd_ms, "bwd_pre_kernel": pre_ms,
+                      "attn_bwd_kernel": main_ms, "bwd_dq_convert_kernel": conv_ms},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": 4 * args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, help="1-based workload index")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-budget-s", type=float, default=120.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

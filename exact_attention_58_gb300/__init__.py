@@ -1,0 +1,243 @@
+"""Fused exact attention for GB300 (sm_103a): Python binding of libgbattn.so.
+
+The functions here carry the names of the C ABI in ``include/gbattn.h`` and
+do argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libgbattn.so``.  PyTorch supplies device memory and streams.
+There is no fallback: if the library has not been built, or an argument is
+unsupported, the call raises.
+
+    import exact_attention_58_gb300 as ea
+    o, lse = ea.attn_fwd(q, k, v, causal=True)
+    dq, dk, dv = ea.attn_bwd(q, k, v, o, do, lse, causal=True)
+
+Tensors are [B, H, N, d], contiguous, on one CUDA device; bf16 (d = 64 or
+128) or, forward only, fp32 with d = 64.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
+    "attn_bwd_main", "attn_bwd_dq_convert", "attn_status_string", "attn_version", "library",
+    "LIB_PATH", "STATUS",
+]
+
+LIB_PATH = _build.LIB_PATH
+
+STATUS = {
+    0: "ATTN_OK",
+    1: "ATTN_ERR_INVALID_ARG",
+    2: "ATTN_ERR_UNSUPPORTED",
+    3: "ATTN_ERR_MISALIGNED",
+    4: "ATTN_ERR_WORKSPACE",
+    5: "ATTN_ERR_CUDA",
+    6: "ATTN_ERR_DEVICE_TIMEOUT",
+}
+_DTYPE = {torch.bfloat16: 0, torch.float32: 1}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    """A non-zero attn_status from the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS.get(self.status, self.status)} "
+                         f"({attn_status_string(self.status)})")
+
+
+def library():
+    """The loaded libgbattn.so.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with exact_attention_58_gb300._build.build() "
+                    "(there is no fallback implementation)")
+            lib = ctypes.CDLL(LIB_PATH)
+            vp, ip, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            f, u64 = ctypes.c_float, ctypes.c_uint64
+            lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, f, ip, vp, f, u64,
+                                     vp, vp]
+            lib.attn_bwd.argtypes = [vp] * 9 + [ip, ip, ip, ip, ip, f, ip, vp, f, u64, vp, sz,
+                                                vp, vp]
+            lib.attn_bwd_workspace_size.argtypes = [ip, ip, ip, ip]
+            lib.attn_bwd_workspace_size.restype = sz
+            lib.attn_bwd_preprocess.argtypes = [vp, vp, vp, ip, ip, ip, ip, ip, vp, sz, vp]
+            lib.attn_bwd_main.argtypes = [vp] * 6 + [ip, ip, ip, ip, ip, f, ip, vp, f, u64, vp,
+                                                     sz, vp, vp]
+            lib.attn_bwd_dq_convert.argtypes = [vp, ip, ip, ip, ip, ip, f, vp, sz, vp]
+            for fn in ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
+                       "attn_bwd_dq_convert"):
+                getattr(lib, fn).restype = ctypes.c_int
+            lib.attn_status_string.argtypes = [ctypes.c_int]
+            lib.attn_status_string.restype = ctypes.c_char_p
+            lib.attn_version.argtypes = []
+            lib.attn_version.restype = ctypes.c_int
+            _lib = lib
+        return _lib
+
+
+def attn_status_string(status: int) -> str:
+    return library().attn_status_string(int(status)).decode()
+
+
+def attn_version() -> int:
+    return int(library().attn_version())
+
+
+def attn_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(library().attn_bwd_workspace_size(B, H, N, d))
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _shape(q: torch.Tensor):
+    if q.dim() != 4:
+        raise ValueError("expected a [B, H, N, d] tensor")
+    return tuple(int(x) for x in q.shape)
+
+
+def _check_like(name: str, t: torch.Tensor, ref: torch.Tensor):
+    if t.shape != ref.shape or t.dtype != ref.dtype or t.device != ref.device:
+        raise ValueError(f"{name} must match q in shape, dtype and device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPE:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    return _DTYPE[t.dtype]
+
+
+def _key_lens(key_lens, q):
+    if key_lens is None:
+        return None
+    if (key_lens.dtype != torch.int32 or key_lens.device != q.device or key_lens.dim() != 1
+            or key_lens.shape[0] != q.shape[0] or not key_lens.is_contiguous()):
+        raise ValueError("key_lens must be a contiguous int32 [B] tensor on q's device")
+    return key_lens
+
+
+def _raise(st: int, where: str):
+    if st != 0:
+        raise AttnError(st, where)
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+def attn_fwd(q, k, v, *, causal: bool = False, key_lens=None, dropout_p: float = 0.0,
+             seed: int = 0, scale: Optional[float] = None, out=None, lse=None,
+             dev_status=None, stream=None):
+    """O, LSE = attention(q, k, v); see include/gbattn.h for the exact contract."""
+    B, H, N, d = _shape(q)
+    _check_like("q", q, q)
+    _check_like("k", k, q)
+    _check_like("v", v, q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _check_like("out", out, q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    kl = _key_lens(key_lens, q)
+    st = library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
+                            _dtype_code(q), float(scale), int(bool(causal)), _ptr(kl),
+                            float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(dev_status),
+                            _stream(stream))
+    _raise(st, "attn_fwd")
+    return out, lse
+
+
+def _workspace(B, H, N, d, workspace, device):
+    need = attn_bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+    return workspace, int(workspace.numel() * workspace.element_size())
+
+
+def attn_bwd(q, k, v, o, do, lse, *, causal: bool = False, key_lens=None,
+             dropout_p: float = 0.0, seed: int = 0, scale: Optional[float] = None, dq=None,
+             dk=None, dv=None, workspace=None, dev_status=None, stream=None):
+    """dQ, dK, dV of attention given the forward's o and lse and the gradient do."""
+    B, H, N, d = _shape(q)
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+        _check_like(name, t, q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_like(name, t, q)
+    ws, ws_bytes = _workspace(B, H, N, d, workspace, q.device)
+    kl = _key_lens(key_lens, q)
+    st = library().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                            _ptr(dk), _ptr(dv), B, H, N, d, _dtype_code(q), float(scale),
+                            int(bool(causal)), _ptr(kl), float(dropout_p),
+                            int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(ws), ws_bytes, _ptr(dev_status),
+                            _stream(stream))
+    _raise(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_preprocess(o, do, lse, workspace, *, stream=None):
+    B, H, N, d = _shape(o)
+    _check_like("do", do, o)
+    st = library().attn_bwd_preprocess(_ptr(o), _ptr(do), _ptr(lse), B, H, N, d,
+                                       _dtype_code(o), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream(stream))
+    _raise(st, "attn_bwd_preprocess")
+
+
+def attn_bwd_main(q, k, v, do, dk, dv, workspace, *, causal=False, key_lens=None,
+                  dropout_p=0.0, seed=0, scale=None, dev_status=None, stream=None):
+    B, H, N, d = _shape(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    kl = _key_lens(key_lens, q)
+    st = library().attn_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dk), _ptr(dv), B, H,
+                                 N, d, _dtype_code(q), float(scale), int(bool(causal)), _ptr(kl),
+                                 float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF,
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _ptr(dev_status), _stream(stream))
+    _raise(st, "attn_bwd_main")
+
+
+def attn_bwd_dq_convert(dq, workspace, *, scale=None, stream=None):
+    B, H, N, d = _shape(dq)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = library().attn_bwd_dq_convert(_ptr(dq), B, H, N, d, _dtype_code(dq), float(scale),
+                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream))
+    _raise(st, "attn_bwd_dq_convert")

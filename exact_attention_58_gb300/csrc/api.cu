@@ -1,0 +1,253 @@
+// api.cu — the C ABI declared in include/gbattn.h: argument validation,
+// TMA tensor-map encoding and kernel dispatch.  Nothing here allocates,
+// frees or synchronises; every launch goes on the caller's stream.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+
+namespace gbattn {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int npad_of(int N) { return ((N + kTileRows - 1) / kTileRows) * kTileRows; }
+
+// Checks shared by every entry point that takes a shape.
+attn_status check_shape(int B, int H, int N, int d, attn_dtype dtype, bool backward) {
+    if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP32) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (dtype == ATTN_DTYPE_FP32 && (backward || d != 64)) return ATTN_ERR_UNSUPPORTED;
+    const long long elems = static_cast<long long>(B) * H * npad_of(N) * d;
+    if (elems >= (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+attn_status check_math(float scale, float dropout_p) {
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (!(dropout_p >= 0.f && dropout_p < 1.f)) return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+uint32_t drop_threshold(float p) {
+    if (!(p > 0.f)) return 0u;
+    const double t = std::floor(static_cast<double>(p) * 4294967296.0);
+    return t >= 4294967295.0 ? 0xFFFFFFFFu : static_cast<uint32_t>(t);
+}
+
+struct Workspace {
+    float* lse2;
+    float* Drow;
+    float* dq_acc;
+};
+
+size_t workspace_bytes_of(int B, int H, int N, int d) {
+    const size_t rows = static_cast<size_t>(B) * H * npad_of(N);
+    return rows * (2 + static_cast<size_t>(d)) * sizeof(float);
+}
+
+Workspace carve(void* ws, int B, int H, int N) {
+    const size_t rows = static_cast<size_t>(B) * H * npad_of(N);
+    float* base = static_cast<float*>(ws);
+    return Workspace{base, base + rows, base + 2 * rows};
+}
+
+attn_status check_workspace(const void* ws, size_t bytes, int B, int H, int N, int d) {
+    if (ws == nullptr || bytes < workspace_bytes_of(B, H, N, d)) return ATTN_ERR_WORKSPACE;
+    if (!aligned16(ws)) return ATTN_ERR_MISALIGNED;
+    return ATTN_OK;
+}
+
+attn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+}  // namespace
+
+bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, bool fp32, int BH, int N, int d) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t es = fp32 ? 4 : 2;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es,
+                                   static_cast<cuuint64_t>(N) * d * es};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(kTileRows), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r =
+        enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace gbattn
+
+using namespace gbattn;
+
+extern "C" {
+
+attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                     int H, int N, int d, attn_dtype dtype, float scale, int causal,
+                     const int32_t* key_lens, float dropout_p, uint64_t seed, int* dev_status,
+                     void* stream) {
+    if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
+    attn_status st = check_shape(B, H, N, d, dtype, false);
+    if (st != ATTN_OK) return st;
+    if ((st = check_math(scale, dropout_p)) != ATTN_OK) return st;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+        return ATTN_ERR_MISALIGNED;
+    const bool fp32 = dtype == ATTN_DTYPE_FP32;
+    CUtensorMap tq, tk, tv;
+    if (!make_tmap_bhnd(&tq, Q, fp32, B * H, N, d) || !make_tmap_bhnd(&tk, K, fp32, B * H, N, d) ||
+        !make_tmap_bhnd(&tv, V, fp32, B * H, N, d))
+        return ATTN_ERR_CUDA;
+    FwdParams p{};
+    p.O = O;
+    p.LSE = LSE;
+    p.key_lens = key_lens;
+    p.dev_status = dev_status;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.nqb = (N + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.out_scale = 1.0f / (1.0f - dropout_p);
+    p.drop_threshold = drop_threshold(dropout_p);
+    p.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFu);
+    p.seed_hi = static_cast<uint32_t>(seed >> 32);
+    return from_cuda(launch_fwd(tq, tk, tv, p, d, fp32, causal != 0, dropout_p > 0.f,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
+    if (check_shape(B, H, N, d, ATTN_DTYPE_BF16, true) != ATTN_OK) return 0;
+    return workspace_bytes_of(B, H, N, d);
+}
+
+attn_status attn_bwd_preprocess(const void* O, const void* dO, const float* LSE, int B, int H,
+                                int N, int d, attn_dtype dtype, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    if (!O || !dO || !LSE) return ATTN_ERR_INVALID_ARG;
+    attn_status st = check_shape(B, H, N, d, dtype, true);
+    if (st != ATTN_OK) return st;
+    if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != ATTN_OK) return st;
+    if (!aligned16(O) || !aligned16(dO) || !aligned16(LSE)) return ATTN_ERR_MISALIGNED;
+    const Workspace w = carve(workspace, B, H, N);
+    return from_cuda(launch_bwd_pre(O, dO, LSE, w.lse2, w.Drow, w.dq_acc, B * H, N, npad_of(N),
+                                    d, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dK,
+                          void* dV, int B, int H, int N, int d, attn_dtype dtype, float scale,
+                          int causal, const int32_t* key_lens, float dropout_p, uint64_t seed,
+                          void* workspace, size_t workspace_bytes, int* dev_status,
+                          void* stream) {
+    if (!Q || !K || !V || !dO || !dK || !dV) return ATTN_ERR_INVALID_ARG;
+    attn_status st = check_shape(B, H, N, d, dtype, true);
+    if (st != ATTN_OK) return st;
+    if ((st = check_math(scale, dropout_p)) != ATTN_OK) return st;
+    if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != ATTN_OK) return st;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(dK) ||
+        !aligned16(dV))
+        return ATTN_ERR_MISALIGNED;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_tmap_bhnd(&tq, Q, false, B * H, N, d) || !make_tmap_bhnd(&tk, K, false, B * H, N, d) ||
+        !make_tmap_bhnd(&tv, V, false, B * H, N, d) || !make_tmap_bhnd(&tdo, dO, false, B * H, N, d))
+        return ATTN_ERR_CUDA;
+    const Workspace w = carve(workspace, B, H, N);
+    BwdParams p{};
+    p.dK = dK;
+    p.dV = dV;
+    p.key_lens = key_lens;
+    p.dev_status = dev_status;
+    p.dq_acc = w.dq_acc;
+    p.lse2 = w.lse2;
+    p.Drow = w.Drow;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.Npad = npad_of(N);
+    p.nkb = (N + kTileRows - 1) / kTileRows;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.scale = scale;
+    p.drop_scale = 1.0f / (1.0f - dropout_p);
+    p.drop_threshold = drop_threshold(dropout_p);
+    p.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFu);
+    p.seed_hi = static_cast<uint32_t>(seed >> 32);
+    return from_cuda(launch_bwd_main(tq, tk, tv, tdo, p, d, causal != 0, dropout_p > 0.f,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+attn_status attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, attn_dtype dtype,
+                                float scale, const void* workspace, size_t workspace_bytes,
+                                void* stream) {
+    if (!dQ) return ATTN_ERR_INVALID_ARG;
+    attn_status st = check_shape(B, H, N, d, dtype, true);
+    if (st != ATTN_OK) return st;
+    if ((st = check_math(scale, 0.f)) != ATTN_OK) return st;
+    if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != ATTN_OK) return st;
+    if (!aligned16(dQ)) return ATTN_ERR_MISALIGNED;
+    const Workspace w = carve(const_cast<void*>(workspace), B, H, N);
+    return from_cuda(launch_bwd_dq_convert(dQ, w.dq_acc, B * H, N, npad_of(N), d, scale,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                     const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
+                     attn_dtype dtype, float scale, int causal, const int32_t* key_lens,
+                     float dropout_p, uint64_t seed, void* workspace, size_t workspace_bytes,
+                     int* dev_status, void* stream) {
+    // Validate everything before the first launch so that errors leave the
+    // outputs untouched.
+    if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
+    attn_status st = check_shape(B, H, N, d, dtype, true);
+    if (st != ATTN_OK) return st;
+    if ((st = check_math(scale, dropout_p)) != ATTN_OK) return st;
+    if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != ATTN_OK) return st;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) ||
+        !aligned16(LSE) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
+        return ATTN_ERR_MISALIGNED;
+    if ((st = attn_bwd_preprocess(O, dO, LSE, B, H, N, d, dtype, workspace, workspace_bytes,
+                                  stream)) != ATTN_OK)
+        return st;
+    if ((st = attn_bwd_main(Q, K, V, dO, dK, dV, B, H, N, d, dtype, scale, causal, key_lens,
+                            dropout_p, seed, workspace, workspace_bytes, dev_status, stream)) !=
+        ATTN_OK)
+        return st;
+    return attn_bwd_dq_convert(dQ, B, H, N, d, dtype, scale, workspace, workspace_bytes, stream);
+}
+
+const char* attn_status_string(attn_status status) {
+    switch (status) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported head dimension, dtype or pass";
+        case ATTN_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+        case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+        case ATTN_ERR_CUDA: return "CUDA runtime or driver call failed";
+        case ATTN_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+int attn_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,576 @@
+// attn_bwd.cu — backward of the fused exact attention for sm_103a.
+//
+// Three launches:
+//   preprocess  D_i = dO_i . O_i, LSE_i * log2(e) into a padded workspace,
+//               and a cleared fp32 dQ accumulator;
+//   main        one CTA per (head, 128-key block): recomputes P tile by tile
+//               from Q, K and the stored log-sum-exp (the recomputation of
+//               "Why FlashAttention Is a Kernel Story", "When it falls down"),
+//               accumulates dK, dV in tensor memory and adds dQ partials into
+//               the workspace;
+//   dq_convert  dQ = scale * accumulator, rounded to bf16.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "philox.cuh"
+#include "ptx.cuh"
+
+namespace gbattn {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// One warp per padded row.  Rows >= N (and rows whose LSE is -inf, which have
+// no valid key) get lse2 = +inf so that the main kernel's P = exp2(s - lse2)
+// is exactly 0 there.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ O,
+                                                      const __nv_bfloat16* __restrict__ dO,
+                                                      const float* __restrict__ LSE,
+                                                      float* __restrict__ lse2,
+                                                      float* __restrict__ Drow,
+                                                      float* __restrict__ dq_acc, int BH, int N,
+                                                      int Npad) {
+    const int lane = threadIdx.x & 31;
+    const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (prow >= static_cast<long long>(BH) * Npad) return;
+    const int bh = static_cast<int>(prow / Npad);
+    const int row = static_cast<int>(prow % Npad);
+    constexpr int PER = D / 32;   // elements per lane
+    float acc = 0.f;
+    if (row < N) {
+        const size_t base = (static_cast<size_t>(bh) * N + row) * D + lane * PER;
+        if constexpr (PER == 4) {
+            const uint2 a = *reinterpret_cast<const uint2*>(O + base);
+            const uint2 g = *reinterpret_cast<const uint2*>(dO + base);
+            acc = bf16lo_to_f32(a.x) * bf16lo_to_f32(g.x) + bf16hi_to_f32(a.x) * bf16hi_to_f32(g.x) +
+                  bf16lo_to_f32(a.y) * bf16lo_to_f32(g.y) + bf16hi_to_f32(a.y) * bf16hi_to_f32(g.y);
+        } else {
+            const uint32_t a = *reinterpret_cast<const uint32_t*>(O + base);
+            const uint32_t g = *reinterpret_cast<const uint32_t*>(dO + base);
+            acc = bf16lo_to_f32(a) * bf16lo_to_f32(g) + bf16hi_to_f32(a) * bf16hi_to_f32(g);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    float* qa = dq_acc + static_cast<size_t>(prow) * D + lane * PER;
+    if constexpr (PER == 4) {
+        *reinterpret_cast<float4*>(qa) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+        *reinterpret_cast<float2*>(qa) = make_float2(0.f, 0.f);
+    }
+    if (lane == 0) {
+        float l2 = INFINITY;
+        if (row < N) {
+            const float lse = LSE[static_cast<size_t>(bh) * N + row];
+            if (lse != -INFINITY) l2 = lse * kLog2e;
+        }
+        lse2[prow] = l2;
+        Drow[prow] = acc;
+    }
+}
+
+// dQ = scale * acc for valid rows; 4 elements per thread.
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(__nv_bfloat16* __restrict__ dQ,
+                                                             const float* __restrict__ dq_acc,
+                                                             long long n4, int N, int Npad, int D,
+                                                             float scale) {
+    const long long i4 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i4 >= n4) return;
+    const long long e = i4 * 4;                 // element index in [BH][N][D]
+    const long long rowg = e / D;               // bh * N + row
+    const int c = static_cast<int>(e % D);
+    const long long bh = rowg / N;
+    const int row = static_cast<int>(rowg % N);
+    const float4 a = *reinterpret_cast<const float4*>(
+        dq_acc + (static_cast<size_t>(bh) * Npad + row) * D + c);
+    uint2 out;
+    out.x = pack_bf16x2(a.x * scale, a.y * scale);
+    out.y = pack_bf16x2(a.z * scale, a.w * scale);
+    *reinterpret_cast<uint2*>(dQ + e) = out;
+}
+
+// ---------------------------------------------------------------------------
+// main kernel
+// ---------------------------------------------------------------------------
+// One CTA per (head, 128-key block j).  K_j and V_j stay in shared memory;
+// the CTA walks the query blocks i (from the diagonal on when causal):
+//   S^T  = K_j Q_i^T          dP^T = V_j dO_i^T          (tcgen05, smem x smem)
+//   P^T  = exp2(S^T scale log2e - LSE_i log2e)           (masked, dropout bits)
+//   dS^T = P^T (dP^T Z/(1-p) - D_i)
+//   dQ_i += dS K_j            (smem x smem, added into the fp32 workspace)
+//   dV_j += (P Z/(1-p))^T dO_i,   dK_j += dS^T Q_i       (P, dS read from TMEM)
+// dK_j (times scale) and dV_j leave the chip once, at the end.
+//
+// Warp roles (320 threads):
+//   warps 0-3  compute: one thread per key row (TMEM lane), builds P and dS
+//   warps 4-7  dQ: one thread per query row, reads dQ from TMEM, adds it
+//              into the workspace with vector atomics
+//   warp  8    TMA producer: K_j, V_j once; Q_i, dO_i, LSE_i, D_i per block
+//   warp  9    MMA issuer
+//
+// Tensor memory (512 columns):
+//   d = 64:  dK [0,64) dV [64,128) S [128,256) dP [256,384) dQ [384,448)
+//   d = 128: dK [0,128) dV [128,256) S [256,384) dP [384,512); P and dS
+//            (bf16 pairs) take the first 64 columns of S and dP, and the two
+//            64-column halves of dQ go in their last 64 columns, so the next
+//            S^T waits until the dQ warps have read dQ out.
+template <int D>
+struct BwdCfg {
+    static constexpr int ROWB = D * 2;
+    static constexpr int NCB = ROWB / 128;
+    static constexpr int TILE = kTileRows * ROWB;
+    static constexpr int CB_BYTES = kTileRows * 128;
+    static constexpr int DS_BYTES = kTileRows * kTileRows * 2;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = TILE;
+    static constexpr int OFF_Q = 2 * TILE;    // 2 stages
+    static constexpr int OFF_DO = 4 * TILE;   // 2 stages
+    static constexpr int OFF_DS = 6 * TILE;
+    static constexpr int OFF_LSE = OFF_DS + DS_BYTES;   // [2][128] float
+    static constexpr int OFF_D = OFF_LSE + 1024;        // [2][128] float
+    static constexpr int OFF_BAR = OFF_D + 1024;
+    static constexpr int SMEM = OFF_BAR + 128;
+    static constexpr int QK_STEPS = ROWB / 32;
+    static constexpr uint32_t C_DK = 0;
+    static constexpr uint32_t C_DV = D;
+    static constexpr uint32_t C_S = 2 * D;
+    static constexpr uint32_t C_DP = 2 * D + 128;
+    static constexpr uint32_t C_DQ = 2 * D + 256;   // d = 64 only
+    static constexpr uint32_t IDESC_SDP = idesc_f32acc(128, 128, false, false, false);
+    static constexpr uint32_t IDESC_DKV = idesc_f32acc(128, D, false, false, true);
+    static constexpr uint32_t IDESC_DQ = idesc_f32acc(128, 64, false, true, true);
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+template <int D, bool kCausal, bool kDropout>
+__global__ void __launch_bounds__(320, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmdO, const BwdParams p) {
+    using C = BwdCfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const int BH = p.B * p.H;
+    int kb, bh;
+    if (kCausal) {   // key block 0 meets every query block: heaviest first
+        kb = static_cast<int>(blockIdx.x) / BH;
+        bh = static_cast<int>(blockIdx.x) % BH;
+    } else {
+        kb = static_cast<int>(blockIdx.x) % p.nkb;
+        bh = static_cast<int>(blockIdx.x) / p.nkb;
+    }
+    const int b = bh / p.H, h = bh % p.H;
+    const int N = p.N;
+    int L = N;
+    if (p.key_lens != nullptr) {
+        const int raw = p.key_lens[b];
+        L = raw < 0 ? 0 : (raw > N ? N : raw);
+        if (raw != L && threadIdx.x == 0 && p.dev_status != nullptr)
+            atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_INVALID_ARG));
+    }
+    const int k0 = kb * kTileRows;
+    const size_t head_off = static_cast<size_t>(bh) * N * D;
+    if (k0 >= L) {   // every key of this block is masked: dK = dV = 0
+        const int rows = min(kTileRows, N - k0);
+        const int n16 = rows * D / 8;   // uint4 per tensor
+        uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dK) + head_off +
+                                             static_cast<size_t>(k0) * D);
+        uint4* dv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dV) + head_off +
+                                             static_cast<size_t>(k0) * D);
+        for (int x = threadIdx.x; x < n16; x += blockDim.x) {
+            dk[x] = make_uint4(0, 0, 0, 0);
+            dv[x] = make_uint4(0, 0, 0, 0);
+        }
+        return;
+    }
+    if ((smem_u32(smem) & 1023u) != 0) {   // the swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0 && p.dev_status != nullptr)
+            atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_CUDA));
+        return;
+    }
+    const int q_begin = kCausal ? kb : 0;
+    const int nq = p.nkb - q_begin;
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* bar_kv = bars + 0;
+    uint64_t* full_q = bars + 1;      // [2]
+    uint64_t* empty_q = bars + 3;     // [2]
+    uint64_t* bar_S = bars + 5;
+    uint64_t* bar_P = bars + 6;
+    uint64_t* bar_dQ = bars + 7;
+    uint64_t* bar_dQfree = bars + 8;
+    uint64_t* bar_dkdv = bars + 9;
+    uint64_t* bar_fin = bars + 10;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 11);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    float* sLSE = reinterpret_cast<float*>(smem + C::OFF_LSE);
+    float* sD = reinterpret_cast<float*>(smem + C::OFF_D);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_kv, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&full_q[s], 1);
+            mbar_init(&empty_q[s], 1);
+        }
+        mbar_init(bar_S, 1);
+        mbar_init(bar_P, kTileRows);
+        mbar_init(bar_dQ, 1);
+        mbar_init(bar_dQfree, kTileRows);
+        mbar_init(bar_dkdv, 1);
+        mbar_init(bar_fin, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(s_tmem, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    if (warp == 8) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            tma_prefetch_desc(&tmdO);
+            mbar_arrive_expect_tx(bar_kv, 2 * C::TILE);
+            for (int cb = 0; cb < C::NCB; ++cb) {
+                tma_load_3d(smem + C::OFF_K + cb * C::CB_BYTES, &tmK, bar_kv, cb * 64, k0, bh);
+                tma_load_3d(smem + C::OFF_V + cb * C::CB_BYTES, &tmV, bar_kv, cb * 64, k0, bh);
+            }
+            int issued = 0;
+            for (int it = 0; it < nq; ++it) {
+                const int stage = it & 1;
+                const uint32_t ph = (it >> 1) & 1;
+                if (!mbar_wait(&empty_q[stage], ph ^ 1, s_abort)) break;
+                const int qi = q_begin + it;
+                mbar_arrive_expect_tx(&full_q[stage], 2 * C::TILE + 1024);
+                for (int cb = 0; cb < C::NCB; ++cb) {
+                    tma_load_3d(smem + C::OFF_Q + stage * C::TILE + cb * C::CB_BYTES, &tmQ,
+                                &full_q[stage], cb * 64, qi * kTileRows, bh);
+                    tma_load_3d(smem + C::OFF_DO + stage * C::TILE + cb * C::CB_BYTES, &tmdO,
+                                &full_q[stage], cb * 64, qi * kTileRows, bh);
+                }
+                const size_t roff = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(qi) * kTileRows;
+                bulk_load(sLSE + stage * kTileRows, p.lse2 + roff, 512, &full_q[stage]);
+                bulk_load(sD + stage * kTileRows, p.Drow + roff, 512, &full_q[stage]);
+                ++issued;
+            }
+            volatile int no_abort = 0;
+            mbar_wait(bar_kv, 0, &no_abort);
+            for (int s = 0; s < 2 && s < issued; ++s) {
+                const int uses = (issued - s + 1) / 2;
+                mbar_wait(&full_q[s], (uses - 1) & 1, &no_abort);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            const uint32_t sK = smem_u32(smem + C::OFF_K);
+            const uint32_t sV = smem_u32(smem + C::OFF_V);
+            const uint32_t sdS = smem_u32(smem + C::OFF_DS);
+            bool ok = mbar_wait(bar_kv, 0, s_abort);
+            for (int it = 0; it < nq && ok; ++it) {
+                const int stage = it & 1;
+                const uint32_t ph = (it >> 1) & 1;
+                const uint32_t sQ = smem_u32(smem + C::OFF_Q + stage * C::TILE);
+                const uint32_t sdO = smem_u32(smem + C::OFF_DO + stage * C::TILE);
+                ok = mbar_wait(&full_q[stage], ph, s_abort);
+                if (ok && D == 128 && it > 0) ok = mbar_wait(bar_dQfree, (it - 1) & 1, s_abort);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < C::QK_STEPS; ++kk) {   // S^T = K Q^T
+                    const uint32_t off = (kk >> 2) * C::CB_BYTES + (kk & 3) * 32;
+                    mma_ss<false>(tmem + C::C_S, sdesc_sw128(sK + off, 16, 1024),
+                                  sdesc_sw128(sQ + off, 16, 1024), C::IDESC_SDP, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < C::QK_STEPS; ++kk) {   // dP^T = V dO^T
+                    const uint32_t off = (kk >> 2) * C::CB_BYTES + (kk & 3) * 32;
+                    mma_ss<false>(tmem + C::C_DP, sdesc_sw128(sV + off, 16, 1024),
+                                  sdesc_sw128(sdO + off, 16, 1024), C::IDESC_SDP, kk > 0);
+                }
+                tc_commit(bar_S);
+                ok = mbar_wait(bar_P, it & 1, s_abort);
+                if (ok && D == 64 && it > 0) ok = mbar_wait(bar_dQfree, (it - 1) & 1, s_abort);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk) {   // dQ = dS K  (K = keys)
+                    const uint64_t ad = sdesc_sw128(sdS + kk * 2048, C::CB_BYTES, 1024);
+                    if constexpr (D == 64) {
+                        mma_ss<false>(tmem + C::C_DQ, ad, sdesc_sw128(sK + kk * 2048, C::CB_BYTES, 1024),
+                                      C::IDESC_DQ, kk > 0);
+                    } else {
+                        mma_ss<false>(tmem + C::C_S + 64, ad,
+                                      sdesc_sw128(sK + kk * 2048, C::CB_BYTES, 1024), C::IDESC_DQ,
+                                      kk > 0);
+                        mma_ss<false>(tmem + C::C_DP + 64, ad,
+                                      sdesc_sw128(sK + C::CB_BYTES + kk * 2048, C::CB_BYTES, 1024),
+                                      C::IDESC_DQ, kk > 0);
+                    }
+                }
+                tc_commit(bar_dQ);
+#pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk)   // dV += P^T dO  (K = queries)
+                    mma_ts<false>(tmem + C::C_DV, tmem + C::C_S + kk * 8,
+                                  sdesc_sw128(sdO + kk * 2048, C::CB_BYTES, 1024), C::IDESC_DKV,
+                                  (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk)   // dK += dS^T Q
+                    mma_ts<false>(tmem + C::C_DK, tmem + C::C_DP + kk * 8,
+                                  sdesc_sw128(sQ + kk * 2048, C::CB_BYTES, 1024), C::IDESC_DKV,
+                                  (it > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(&empty_q[stage]);
+            }
+            if (ok) tc_commit(bar_dkdv);
+            tc_commit(bar_fin);
+            volatile int no_abort = 0;
+            mbar_wait(bar_fin, 0, &no_abort);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ================= compute: P and dS, one key row per thread =================
+        const int r = warp * 32 + lane;
+        const int j = k0 + r;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const bool row_valid = j < L;
+        uint8_t* sdS = smem + C::OFF_DS;
+        bool ok = true;
+        for (int it = 0; it < nq; ++it) {
+            const int stage = it & 1;
+            const uint32_t ph = (it >> 1) & 1;
+            const int qi = q_begin + it;
+            if (!mbar_wait_warp(bar_S, it & 1, s_abort) ||
+                !mbar_wait_warp(&full_q[stage], ph, s_abort)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float* lse_s = sLSE + stage * kTileRows;
+            const float* d_s = sD + stage * kTileRows;
+            const bool diag = kCausal && (qi == kb);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sv[32], dpv[32];
+                tmem_ld32(tl + C::C_S + 32 * c, sv);
+                tmem_ld32(tl + C::C_DP + 32 * c, dpv);
+                tmem_ld_wait();
+                reg_fence(sv);
+                reg_fence(dpv);
+                uint32_t keep = 0xFFFFFFFFu;   // bit e: column 32c+e kept
+                if constexpr (kDropout) {
+                    keep = 0u;
+                    const int a = lane & 3;
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const int iq = qi * kTileRows + 32 * c + 4 * g + a;
+                        uint32_t v = dropout_keep4(p.seed_lo, p.seed_hi, p.drop_threshold, iq,
+                                                   j & ~3, h, b)
+                                     << (4 * a);
+                        v |= __shfl_xor_sync(0xffffffffu, v, 1);
+                        v |= __shfl_xor_sync(0xffffffffu, v, 2);
+                        const int e = lane & 3;   // this thread's key within the quad
+#pragma unroll
+                        for (int a2 = 0; a2 < 4; ++a2)
+                            keep |= ((v >> (4 * a2 + e)) & 1u) << (4 * g + a2);
+                    }
+                }
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float pd[2], ds[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int col = 32 * c + 2 * e + u;
+                        const int iq = qi * kTileRows + col;
+                        float pr = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), p.scale_log2,
+                                                   -lse_s[col]));
+                        const bool valid = row_valid && (!diag || j <= iq);
+                        pr = valid ? pr : 0.f;
+                        float dp = __uint_as_float(dpv[2 * e + u]);
+                        float pdrop = pr;
+                        if constexpr (kDropout) {
+                            const bool z = (keep >> (2 * e + u)) & 1u;
+                            pdrop = z ? pr * p.drop_scale : 0.f;
+                            dp = z ? dp * p.drop_scale : 0.f;
+                        }
+                        pd[u] = pdrop;
+                        ds[u] = pr * (dp - d_s[col]);
+                    }
+                    pk[e] = pack_bf16x2(pd[0], pd[1]);
+                    dk[e] = pack_bf16x2(ds[0], ds[1]);
+                }
+                tmem_st16(tl + C::C_S + 16 * c, pk);
+                tmem_st16(tl + C::C_DP + 16 * c, dk);
+                // dS (bf16) into shared memory as the dQ MMA's A operand: query
+                // index innermost (MN-major), 128-byte swizzle.
+                uint8_t* rowp = sdS + (c >> 1) * C::CB_BYTES + r * 128;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int chunk = ((c & 1) * 4 + u) ^ (r & 7);
+                    *reinterpret_cast<uint4*>(rowp + chunk * 16) =
+                        make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+                }
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_P);
+        }
+        // ---- epilogue: dK = scale * acc, dV = acc, to bf16 ----
+        if (ok) {
+            ok = mbar_wait_warp(bar_dkdv, 0, s_abort);
+            tc_fence_after();
+        }
+        if (ok) {
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t a[32], v[32];
+                tmem_ld32(tl + C::C_DK + 32 * c, a);
+                tmem_ld32(tl + C::C_DV + 32 * c, v);
+                tmem_ld_wait();
+                reg_fence(a);
+                reg_fence(v);
+                if (j < N) {
+                    const size_t off = head_off + static_cast<size_t>(j) * D + 32 * c;
+                    uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dK) + off);
+                    uint4* dv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dV) + off);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t wk[4], wv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            wk[e] = pack_bf16x2(__uint_as_float(a[8 * q4 + 2 * e]) * p.scale,
+                                                __uint_as_float(a[8 * q4 + 2 * e + 1]) * p.scale);
+                            wv[e] = pack_bf16x2(__uint_as_float(v[8 * q4 + 2 * e]),
+                                                __uint_as_float(v[8 * q4 + 2 * e + 1]));
+                        }
+                        dk[q4] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+                        dv[q4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    }
+                }
+            }
+        }
+    } else {
+        // ================= dQ: one query row per thread =================
+        const int rq = (warp - 4) * 32 + lane;
+        const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        for (int it = 0; it < nq; ++it) {
+            const int i = (q_begin + it) * kTileRows + rq;
+            if (!mbar_wait_warp(bar_dQ, it & 1, s_abort)) break;
+            tc_fence_after();
+            uint32_t x[D / 32][32];
+            if constexpr (D == 64) {
+                tmem_ld32(tl + C::C_DQ, x[0]);
+                tmem_ld32(tl + C::C_DQ + 32, x[1]);
+            } else {
+                tmem_ld32(tl + C::C_S + 64, x[0]);
+                tmem_ld32(tl + C::C_S + 96, x[1]);
+                tmem_ld32(tl + C::C_DP + 64, x[2]);
+                tmem_ld32(tl + C::C_DP + 96, x[3]);
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) reg_fence(x[c]);
+            tc_fence_before();
+            mbar_arrive(bar_dQfree);
+            if (i < N) {
+                float4* dst = reinterpret_cast<float4*>(
+                    p.dq_acc + (static_cast<size_t>(bh) * p.Npad + i) * D);
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        atomicAdd(dst + c * 8 + v,
+                                  make_float4(__uint_as_float(x[c][4 * v]),
+                                              __uint_as_float(x[c][4 * v + 1]),
+                                              __uint_as_float(x[c][4 * v + 2]),
+                                              __uint_as_float(x[c][4 * v + 3])));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) tmem_dealloc(tmem, 512);
+    if (threadIdx.x == 0 && *s_abort && p.dev_status != nullptr)
+        atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_DEVICE_TIMEOUT));
+}
+
+template <int D, bool kCausal, bool kDropout>
+cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+    using C = BwdCfg<D>;
+    auto kern = attn_bwd_kernel<D, kCausal, kDropout>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const unsigned grid = static_cast<unsigned>(p.nkb) * static_cast<unsigned>(p.B * p.H);
+    kern<<<grid, 320, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t dispatch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const BwdParams& p, bool causal, bool dropout,
+                         cudaStream_t s) {
+    if (causal)
+        return dropout ? launch_bwd_t<D, true, true>(tq, tk, tv, tdo, p, s)
+                       : launch_bwd_t<D, true, false>(tq, tk, tv, tdo, p, s);
+    return dropout ? launch_bwd_t<D, false, true>(tq, tk, tv, tdo, p, s)
+                   : launch_bwd_t<D, false, false>(tq, tk, tv, tdo, p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(const void* O, const void* dO, const float* LSE, float* lse2,
+                           float* Drow, float* dq_acc, int BH, int N, int Npad, int d,
+                           cudaStream_t stream) {
+    const long long rows = static_cast<long long>(BH) * Npad;
+    const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+    if (d == 64)
+        bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(O),
+                                                     static_cast<const __nv_bfloat16*>(dO), LSE,
+                                                     lse2, Drow, dq_acc, BH, N, Npad);
+    else if (d == 128)
+        bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(O),
+                                                      static_cast<const __nv_bfloat16*>(dO), LSE,
+                                                      lse2, Drow, dq_acc, BH, N, Npad);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_convert(void* dQ, const float* dq_acc, int BH, int N, int Npad, int d,
+                                  float scale, cudaStream_t stream) {
+    const long long n4 = static_cast<long long>(BH) * N * d / 4;
+    const unsigned grid = static_cast<unsigned>((n4 + 255) / 256);
+    bwd_dq_convert_kernel<<<grid, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(dQ), dq_acc, n4,
+                                                    N, Npad, d, scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdParams& p, int d, bool causal,
+                            bool dropout, cudaStream_t stream) {
+    if (d == 64) return dispatch_bwd<64>(tq, tk, tv, tdo, p, causal, dropout, stream);
+    if (d == 128) return dispatch_bwd<128>(tq, tk, tv, tdo, p, causal, dropout, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gbattn

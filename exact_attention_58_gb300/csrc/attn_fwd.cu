@@ -1,0 +1,496 @@
+// attn_fwd.cu — fused exact-attention forward for sm_103a.
+//
+// One CTA owns 256 query rows (two 128-row tiles, A and B) of one (b, h) head
+// and walks the key/value sequence in 128-row blocks, keeping everything on
+// chip: the online-softmax recurrence of "Why FlashAttention Is a Kernel
+// Story" (section "Tiling": running row max m, running denominator l, output
+// rescaled when m grows, O / l at the end) with S = Q K^T and O += P V on the
+// tcgen05 tensor cores.  Only O and the per-row log-sum-exp reach HBM.
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax for tile A, one thread per query row (TMEM lane)
+//   warps 4-7  softmax for tile B
+//   warp  8    TMA producer: Q once, then K_j, V_j into a ring of smem slots
+//   warp  9    MMA issuer: S_t = Q_t K_j^T (both operands in smem) and
+//              O_t += P_t V_j (P read from tensor memory, V from smem)
+//
+// Tensor memory (512 columns x 128 lanes x 32 bit):
+//   [0,128)   S_A, later P_A (bf16 pairs in the first 64 columns, or fp32)
+//   [128,256) S_B / P_B
+//   [256, 256+d) O_A,  [256+d, 256+2d) O_B   (fp32 accumulators)
+// P aliases S: the MMA warp issues S_t(j+1) only after O_t += P_t(j) V_j,
+// and tcgen05 MMAs from one thread execute in issue order.
+//
+// Rescaling follows the recurrence exactly but lazily: a row keeps its
+// reference max until the block max exceeds it by more than 8 (log2 units),
+// so P <= 2^8 and O, l stay consistent with the same reference; the final
+// O / l is unchanged.
+//
+// Every wait is bounded (kWaitLimitNs); on expiry the CTA drains its own
+// TMA loads and MMAs, frees tensor memory and reports
+// ATTN_ERR_DEVICE_TIMEOUT through dev_status.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "philox.cuh"
+#include "ptx.cuh"
+
+namespace gbattn {
+namespace {
+
+template <int D, bool kTF32>
+struct FwdCfg {
+    static constexpr int ES = kTF32 ? 4 : 2;               // element bytes
+    static constexpr int ROWB = D * ES;                    // bytes per row
+    static constexpr int NCB = ROWB / 128;                 // 128-byte column blocks
+    static constexpr int BOXW = 128 / ES;                  // elements per column block
+    static constexpr int TILE = kTileRows * ROWB;          // bytes per 128-row tile
+    static constexpr int CB_BYTES = kTileRows * 128;       // bytes per column block
+    static constexpr int NSLOT = (ROWB == 128) ? 8 : 4;    // K/V ring slots
+    static constexpr int KSTEP = 32 / ES;                  // K elements per MMA
+    static constexpr int QK_STEPS = ROWB / 32;             // MMAs per S tile
+    static constexpr int PV_STEPS = kTileRows / KSTEP;     // MMAs per P V
+    static constexpr int SMEM = (2 + NSLOT) * TILE + 1024 /*barriers*/ + 1024 /*align*/;
+    static constexpr uint32_t IDESC_QK = idesc_f32acc(128, 128, kTF32, false, false);
+    static constexpr uint32_t IDESC_PV = idesc_f32acc(128, D, kTF32, false, true);
+    static_assert(ROWB == 128 || ROWB == 256, "tile rows must be 128 or 256 bytes");
+};
+
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int D, bool kTF32, bool kCausal, bool kDropout>
+__global__ void __launch_bounds__(320, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+    using C = FwdCfg<D, kTF32>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = smem;                                   // 2 tiles
+    uint8_t* sKV = smem + 2 * C::TILE;                    // NSLOT tiles
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (2 + C::NSLOT) * C::TILE);
+    uint64_t* bar_q = bars;
+    uint64_t* full = bars + 1;
+    uint64_t* empty = full + C::NSLOT;
+    uint64_t* bar_s = empty + C::NSLOT;   // [2]
+    uint64_t* bar_p = bar_s + 2;          // [2]
+    uint64_t* bar_o = bar_p + 2;          // [2]
+    uint64_t* bar_fin = bar_o + 2;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_fin + 1);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- which 256 query rows of which head ----
+    const int BH = p.B * p.H;
+    int qb, bh;
+    if (kCausal) {   // heaviest query blocks first
+        qb = p.nqb - 1 - static_cast<int>(blockIdx.x) / BH;
+        bh = static_cast<int>(blockIdx.x) % BH;
+    } else {         // neighbouring CTAs share a head's K/V in L2
+        qb = static_cast<int>(blockIdx.x) % p.nqb;
+        bh = static_cast<int>(blockIdx.x) / p.nqb;
+    }
+    const int b = bh / p.H, h = bh % p.H;
+    const int N = p.N;
+    int L = N;
+    if (p.key_lens != nullptr) {
+        const int raw = p.key_lens[b];
+        L = raw < 0 ? 0 : (raw > N ? N : raw);
+        if (raw != L && threadIdx.x == 0 && p.dev_status != nullptr)
+            atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_INVALID_ARG));
+    }
+    const int q0 = qb * kFwdRowsPerCta;
+    const int nkv_all = (L + kTileRows - 1) / kTileRows;
+    int nkv_t[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int first = q0 + t * kTileRows;
+        if (first >= N) {
+            nkv_t[t] = 0;
+        } else if (kCausal) {
+            const int last = min(first + kTileRows - 1, N - 1);
+            nkv_t[t] = min(nkv_all, last / kTileRows + 1);
+        } else {
+            nkv_t[t] = nkv_all;
+        }
+    }
+    const int nkv = max(nkv_t[0], nkv_t[1]);
+
+    // ---- set-up ----
+    if (threadIdx.x == 0) {
+        mbar_init(bar_q, 1);
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&bar_s[t], 1);
+            mbar_init(&bar_p[t], kTileRows);
+            mbar_init(&bar_o[t], 1);
+        }
+        mbar_init(bar_fin, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(s_tmem, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    if (warp == 8) {
+        // ================= TMA producer =================
+        if (lane == 0 && nkv > 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            const int ntiles = (nkv_t[1] > 0) ? 2 : 1;
+            mbar_arrive_expect_tx(bar_q, ntiles * C::TILE);
+            for (int t = 0; t < ntiles; ++t)
+                for (int cb = 0; cb < C::NCB; ++cb)
+                    tma_load_3d(sQ + t * C::TILE + cb * C::CB_BYTES, &tmQ, bar_q, cb * C::BOXW,
+                                q0 + t * kTileRows, bh);
+            int seq = 0;
+            bool ok = true;
+            for (int j = 0; j < nkv && ok; ++j) {
+                for (int which = 0; which < 2; ++which) {
+                    const int slot = seq % C::NSLOT;
+                    const uint32_t ph = (seq / C::NSLOT) & 1;
+                    if (!mbar_wait(&empty[slot], ph ^ 1, s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[slot], C::TILE);
+                    const CUtensorMap* m = which ? &tmV : &tmK;
+                    for (int cb = 0; cb < C::NCB; ++cb)
+                        tma_load_3d(sKV + slot * C::TILE + cb * C::CB_BYTES, m, &full[slot],
+                                    cb * C::BOXW, j * kTileRows, bh);
+                    ++seq;
+                }
+            }
+            // Drain: every load this thread issued has landed before teardown.
+            volatile int no_abort = 0;
+            mbar_wait(bar_q, 0, &no_abort);
+            for (int s = 0; s < C::NSLOT && s < seq; ++s) {
+                const int uses = (seq - s + C::NSLOT - 1) / C::NSLOT;
+                mbar_wait(&full[s], (uses - 1) & 1, &no_abort);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // ================= MMA issuer =================
+        if (lane == 0 && nkv > 0) {
+            const uint32_t sq[2] = {smem_u32(sQ), smem_u32(sQ + C::TILE)};
+            const uint32_t skv = smem_u32(sKV);
+            auto issue_qk = [&](int t, int slot) {
+                const uint32_t d_tmem = tmem + 128u * t;
+#pragma unroll
+                for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::CB_BYTES + (kk & 3) * 32;
+                    const uint64_t ad = sdesc_sw128(sq[t] + off, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(skv + slot * C::TILE + off, 16, 1024);
+                    mma_ss<kTF32>(d_tmem, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, int slot, bool accumulate) {
+                const uint32_t d_tmem = tmem + 256u + D * t;
+                const uint32_t a_tmem = tmem + 128u * t;
+#pragma unroll
+                for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+                    const uint64_t bd = sdesc_sw128(skv + slot * C::TILE + kk * C::KSTEP * 128,
+                                                    C::CB_BYTES, 1024);
+                    mma_ts<kTF32>(d_tmem, a_tmem + kk * 8, bd, C::IDESC_PV,
+                                  (accumulate || kk > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = mbar_wait(bar_q, 0, s_abort);
+            tc_fence_after();
+            int seq = 0;
+            int v_slot = 0;
+            uint32_t v_phase = 0;
+            bool v_ready = false;
+            for (int j = 0; j < nkv && ok; ++j) {
+                const int kslot = seq % C::NSLOT;
+                const uint32_t kph = (seq / C::NSLOT) & 1;
+                ++seq;
+                const int next_v_slot = seq % C::NSLOT;
+                const uint32_t next_v_phase = (seq / C::NSLOT) & 1;
+                ++seq;
+                bool k_ready = false;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    const bool qk = j < nkv_t[t];
+                    const bool last_pv = (j == nkv_t[t]) && j > 0;
+                    if ((qk && j > 0) || last_pv) {   // O_t += P_t(j-1) V_{j-1}
+                        ok = mbar_wait(&bar_p[t], (j - 1) & 1, s_abort);
+                        if (ok && !v_ready) {
+                            ok = mbar_wait(&full[v_slot], v_phase, s_abort);
+                            v_ready = true;
+                        }
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(t, v_slot, j - 1 > 0);
+                        if (last_pv) tc_commit(&bar_o[t]);
+                    }
+                    if (qk) {                         // S_t = Q_t K_j^T
+                        if (!k_ready) {
+                            ok = mbar_wait(&full[kslot], kph, s_abort);
+                            k_ready = true;
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        issue_qk(t, kslot);
+                        tc_commit(&bar_s[t]);
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&empty[kslot]);
+                if (j > 0) tc_commit(&empty[v_slot]);
+                v_slot = next_v_slot;
+                v_phase = next_v_phase;
+                v_ready = false;
+            }
+            for (int t = 0; t < 2 && ok; ++t) {   // tiles whose last block is nkv-1
+                if (nkv_t[t] != nkv) continue;
+                ok = mbar_wait(&bar_p[t], (nkv - 1) & 1, s_abort);
+                if (ok && !v_ready) {
+                    ok = mbar_wait(&full[v_slot], v_phase, s_abort);
+                    v_ready = true;
+                }
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(t, v_slot, nkv - 1 > 0);
+                tc_commit(&bar_o[t]);
+            }
+            // Drain: no MMA of this CTA is in flight at teardown.
+            tc_commit(bar_fin);
+            volatile int no_abort = 0;
+            mbar_wait(bar_fin, 0, &no_abort);
+        }
+        __syncwarp();
+    } else {
+        // ================= softmax (warps 0-7) =================
+        const int t = warp >> 2;
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const int row = q0 + t * kTileRows + r;
+        const int ntile = nkv_t[t];
+        const int tile_first_row = q0 + t * kTileRows;
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const uint32_t t_S = t_lane + 128u * t;
+        const uint32_t t_O = t_lane + 256u + D * t;
+        float m_ref = -INFINITY;   // reference max, log2 units of scaled scores
+        float l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntile; ++j) {
+            if (!mbar_wait_warp(&bar_s[t], j & 1, s_abort)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(t_S + 32 * c, sr[c]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+
+            const int k0 = j * kTileRows;
+            const bool tile_mask = (k0 + kTileRows > L) ||
+                                   (kCausal && k0 + kTileRows - 1 > tile_first_row);
+            if (tile_mask) {
+                const int lim = (kCausal ? min(L, row + 1) : L) - k0;
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c >= lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
+            const float m_new = fmaxf(m_ref, mx * p.scale_log2);
+            const bool want = (m_ref != -INFINITY) && (m_new > m_ref + kRescaleThreshold);
+            const bool warp_rescale = __any_sync(0xffffffffu, want);
+            float alpha = 1.f;
+            if (m_ref == -INFINITY) {
+                m_ref = m_new;   // O and l are still zero: adopt without rescaling
+            } else if (warp_rescale) {
+                alpha = ex2_approx(m_ref - m_new);
+                m_ref = m_new;
+            }
+            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+
+            float rowsum = 0.f;
+            if constexpr (!kTF32) {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {   // 4 keys per group
+                        const int c = 32 * cc + 4 * g;
+                        uint32_t keep = 0xFu;
+                        if constexpr (kDropout)
+                            keep = dropout_keep4(p.seed_lo, p.seed_hi, p.drop_threshold, row,
+                                                 k0 + c, h, b);
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float x0 = ex2_approx(
+                                fmaf(__uint_as_float(sr[cc][4 * g + 2 * e]), p.scale_log2, neg_m));
+                            const float x1 = ex2_approx(fmaf(
+                                __uint_as_float(sr[cc][4 * g + 2 * e + 1]), p.scale_log2, neg_m));
+                            uint32_t u = pack_bf16x2(x0, x1);
+                            rowsum += bf16lo_to_f32(u) + bf16hi_to_f32(u);
+                            if constexpr (kDropout) {
+                                const uint32_t km = ((keep >> (2 * e)) & 1u ? 0x0000FFFFu : 0u) |
+                                                    ((keep >> (2 * e + 1)) & 1u ? 0xFFFF0000u : 0u);
+                                u &= km;
+                            }
+                            pk[2 * g + e] = u;
+                        }
+                    }
+                    tmem_st16(t_S + 16 * cc, pk);
+                }
+            } else {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t pf[32];
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const int c = 32 * cc + 4 * g;
+                        uint32_t keep = 0xFu;
+                        if constexpr (kDropout)
+                            keep = dropout_keep4(p.seed_lo, p.seed_hi, p.drop_threshold, row,
+                                                 k0 + c, h, b);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float x = ex2_approx(
+                                fmaf(__uint_as_float(sr[cc][4 * g + e]), p.scale_log2, neg_m));
+                            rowsum += x;
+                            pf[4 * g + e] = ((keep >> e) & 1u) ? __float_as_uint(x) : 0u;
+                        }
+                    }
+                    tmem_st32(t_S + 32 * cc, pf);
+                }
+            }
+            l = l * alpha + rowsum;
+            if (warp_rescale && j > 0) {   // O row *= alpha (PV of block j-1 is complete)
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(t_O + 32 * c, o);
+                    tmem_ld_wait();
+                    reg_fence(o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(t_O + 32 * c, o);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bar_p[t]);
+        }
+        // ---- epilogue: O = acc / l (times 1/(1-p)), LSE = (m + log2 l) ln 2 ----
+        if (ok && ntile > 0) {
+            ok = mbar_wait_warp(&bar_o[t], 0, s_abort);
+            tc_fence_after();
+        }
+        if (ok) {
+            const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
+            const size_t row_off = (static_cast<size_t>(bh) * N + row) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                if (ntile > 0) {
+                    tmem_ld32(t_O + 32 * c, o);
+                    tmem_ld_wait();
+                    reg_fence(o);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+                if (row < N) {
+                    if constexpr (kTF32) {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.O) + row_off + 32 * c);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv,
+                                                 __uint_as_float(o[4 * v + 1]) * inv,
+                                                 __uint_as_float(o[4 * v + 2]) * inv,
+                                                 __uint_as_float(o[4 * v + 3]) * inv);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            static_cast<__nv_bfloat16*>(p.O) + row_off + 32 * c);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                w[e] = pack_bf16x2(__uint_as_float(o[8 * v + 2 * e]) * inv,
+                                                   __uint_as_float(o[8 * v + 2 * e + 1]) * inv);
+                            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+            }
+            if (row < N)
+                p.LSE[static_cast<size_t>(bh) * N + row] =
+                    (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        }
+    }
+
+    // ---- teardown ----
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) tmem_dealloc(tmem, kTmemCols);
+    if (threadIdx.x == 0 && *s_abort && p.dev_status != nullptr)
+        atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_DEVICE_TIMEOUT));
+}
+
+template <int D, bool kTF32, bool kCausal, bool kDropout>
+cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const FwdParams& p, cudaStream_t stream) {
+    using C = FwdCfg<D, kTF32>;
+    auto kern = attn_fwd_kernel<D, kTF32, kCausal, kDropout>;
+    static bool configured = false;   // benign race: the attribute call is idempotent
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const unsigned grid = static_cast<unsigned>(p.nqb) * static_cast<unsigned>(p.B * p.H);
+    kern<<<grid, 320, C::SMEM, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+template <int D, bool kTF32>
+cudaError_t dispatch_mask(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const FwdParams& p, bool causal, bool dropout, cudaStream_t s) {
+    if (causal)
+        return dropout ? launch_fwd_t<D, kTF32, true, true>(tq, tk, tv, p, s)
+                       : launch_fwd_t<D, kTF32, true, false>(tq, tk, tv, p, s);
+    return dropout ? launch_fwd_t<D, kTF32, false, true>(tq, tk, tv, p, s)
+                   : launch_fwd_t<D, kTF32, false, false>(tq, tk, tv, p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, int d, bool fp32, bool causal, bool dropout,
+                       cudaStream_t stream) {
+    if (fp32) {
+        if (d == 64) return dispatch_mask<64, true>(tq, tk, tv, p, causal, dropout, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (d == 64) return dispatch_mask<64, false>(tq, tk, tv, p, causal, dropout, stream);
+    if (d == 128) return dispatch_mask<128, false>(tq, tk, tv, p, causal, dropout, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gbattn

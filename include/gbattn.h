@@ -1,0 +1,153 @@
+/*
+ * gbattn.h — C ABI of the fused exact-attention library (libgbattn.so).
+ *
+ * The library computes exact scaled-dot-product attention
+ *
+ *     O = dropout(softmax(scale * Q K^T + mask)) V
+ *
+ * on one GPU (sm_103a) as a single tiled kernel that never writes the N x N
+ * score or probability matrix to device memory, and the matching backward
+ * pass that recomputes the probabilities tile by tile from Q, K and the
+ * stored log-sum-exp.  The operation is the attention chain of
+ * anthology-of-the-sota practice SOTA-114 ("The general form of the practice
+ * above it": matmul, scale, mask, softmax, dropout, matmul fused into one
+ * kernel) computed with the online-softmax tiling of "Why FlashAttention Is a
+ * Kernel Story" (section "Tiling: fitting the work inside SRAM"); the
+ * backward's recomputation is the one that page describes under "When it falls
+ * down" (backward-pass complexity).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  Layout     Q, K, V, O, dO, dQ, dK, dV are contiguous [B, H, N, d] arrays,
+ *             d innermost (row-major), one element type for all of them.
+ *             LSE is a contiguous float [B, H, N] array.  key_lens is an
+ *             int32 [B] array.  Every pointer is a DEVICE pointer.
+ *  Alignment  Every tensor pointer must be 16-byte aligned
+ *             (ATTN_ERR_MISALIGNED otherwise).
+ *  Types      ATTN_DTYPE_BF16: bf16 storage, bf16 x bf16 products with fp32
+ *             accumulation.  ATTN_DTYPE_FP32: fp32 storage, TF32 products
+ *             with fp32 accumulation (forward only, d = 64).
+ *  Shapes     d in {64, 128}; B, H, N >= 1; B*H*N*d < 2^31 elements per
+ *             tensor.  Anything else returns ATTN_ERR_UNSUPPORTED or
+ *             ATTN_ERR_INVALID_ARG: the library never falls back to another
+ *             implementation.
+ *  Mask       key j of sequence b is attended iff j < key_lens[b] (all N keys
+ *             when key_lens is NULL) and, when causal != 0, j <= i.  A query
+ *             row with no valid key gets O = 0 and LSE = -inf (and zero
+ *             gradients).  key_lens values outside [0, N] are clamped on the
+ *             device and reported as ATTN_ERR_INVALID_ARG through dev_status.
+ *  Scale      scale must be finite and > 0 (1/sqrt(d) is the usual choice).
+ *  Dropout    0 <= dropout_p < 1.  Kept probabilities are multiplied by
+ *             1/(1 - dropout_p); the softmax denominator and LSE use the
+ *             undropped probabilities.  The keep bit of score (i, j) of head
+ *             (b, h) is word j&3 of Philox4x32-10 (Salmon et al., SC'11) at
+ *             counter (i, j>>2, h, b) under key (lo32(seed), hi32(seed)); the
+ *             score is dropped iff that word < floor(dropout_p * 2^32).
+ *             attn_bwd must get the same dropout_p, seed, causal and key_lens
+ *             as the attn_fwd whose O and LSE it is given.
+ *  Ownership  The caller owns every buffer, including the workspace.  The
+ *             library never allocates, frees or synchronises.
+ *  Streams    stream is a cudaStream_t (NULL = the legacy default stream).
+ *             Work is enqueued asynchronously; outputs are valid once the
+ *             stream has reached the work.
+ *  Errors     Argument errors are returned before anything is enqueued, with
+ *             the outputs untouched.  A failed launch returns ATTN_ERR_CUDA.
+ *             Errors detected on the device (a bounded wait that expired, an
+ *             out-of-range key length) are written to *dev_status (a device
+ *             int, 0 = OK) when dev_status is not NULL; the kernel then exits
+ *             cleanly and leaves the affected outputs unspecified.
+ *  Threads    Every entry point is thread-safe.
+ */
+#ifndef GBATTN_H
+#define GBATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,    /* NULL pointer, bad size, scale, dropout_p or key length */
+    ATTN_ERR_UNSUPPORTED = 2,    /* d, dtype or pass not built (never a silent fallback) */
+    ATTN_ERR_MISALIGNED = 3,     /* a tensor pointer is not 16-byte aligned */
+    ATTN_ERR_WORKSPACE = 4,      /* workspace NULL or smaller than attn_bwd_workspace_size */
+    ATTN_ERR_CUDA = 5,           /* a CUDA runtime or driver call failed */
+    ATTN_ERR_DEVICE_TIMEOUT = 6  /* (dev_status only) a bounded device-side wait expired */
+} attn_status;
+
+typedef enum {
+    ATTN_DTYPE_BF16 = 0,
+    ATTN_DTYPE_FP32 = 1
+} attn_dtype;
+
+/*
+ * Forward pass.
+ *   Q, K, V   in   [B, H, N, d]
+ *   O         out  [B, H, N, d]  (same dtype as Q)
+ *   LSE       out  [B, H, N] float: natural log of the sum over valid keys of
+ *                  exp(scale * q_i . k_j) (-inf for a row with no valid key)
+ * One kernel launch.  Supported: bf16 with d in {64, 128}; fp32 (TF32
+ * products) with d = 64.
+ */
+attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                     int B, int H, int N, int d, attn_dtype dtype, float scale, int causal,
+                     const int32_t* key_lens, float dropout_p, uint64_t seed,
+                     int* dev_status, void* stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs: per head, the row terms
+ * D_i = dO_i . O_i and the log-sum-exp in base 2 (two floats per row) and an
+ * fp32 accumulator for dQ, with N rounded up to a multiple of 128.
+ * Returns 0 for arguments attn_bwd would reject.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass: given the forward's inputs, its O and LSE and the incoming
+ * gradient dO, writes dQ, dK, dV (same dtype and layout as Q).  bf16 only,
+ * d in {64, 128}.  workspace must hold attn_bwd_workspace_size(B, H, N, d)
+ * bytes (16-byte aligned); its contents on entry do not matter.  Enqueues
+ * three launches: attn_bwd_preprocess, attn_bwd_main, attn_bwd_dq_convert.
+ */
+attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
+                     const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                     int B, int H, int N, int d, attn_dtype dtype, float scale, int causal,
+                     const int32_t* key_lens, float dropout_p, uint64_t seed,
+                     void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
+
+/*
+ * The three stages of attn_bwd, exported so that a caller can enqueue (and
+ * time) them one by one.  Same arguments and rules as attn_bwd; calling the
+ * three in this order on one stream with one workspace is exactly attn_bwd.
+ *   preprocess: D_i = dO_i . O_i and LSE_i * log2(e) into the workspace;
+ *               clears the dQ accumulator.
+ *   main:       recomputes P tile by tile; writes dK, dV; accumulates dQ
+ *               (unscaled) into the workspace.
+ *   dq_convert: dQ = scale * accumulator, rounded to the output dtype.
+ */
+attn_status attn_bwd_preprocess(const void* O, const void* dO, const float* LSE,
+                                int B, int H, int N, int d, attn_dtype dtype,
+                                void* workspace, size_t workspace_bytes, void* stream);
+attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO,
+                          void* dK, void* dV, int B, int H, int N, int d, attn_dtype dtype,
+                          float scale, int causal, const int32_t* key_lens, float dropout_p,
+                          uint64_t seed, void* workspace, size_t workspace_bytes,
+                          int* dev_status, void* stream);
+attn_status attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, attn_dtype dtype,
+                                float scale, const void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* attn_status_string(attn_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBATTN_H */

@@ -14,6 +14,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 import threading
 
@@ -21,7 +22,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
-_BUILD_DIR = os.path.join(_HERE, "_build")
+_BUILD_DIR = os.path.join(_HERE, "_build", platform.machine())
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +71,11 @@ def _bind(lib):
     lib.oracle_heads_fwd.restype = ctypes.c_int
     lib.oracle_heads_bwd.argtypes = [_dp] * 8 + heads_common
     lib.oracle_heads_bwd.restype = ctypes.c_int
+    lib.oracle_heads_rows_fwd_bwd.argtypes = (
+        [_dp] * 4 + [ctypes.c_int, _ip, _ip, _ip, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                     ctypes.c_int, ctypes.c_double, ctypes.c_uint64, ctypes.c_int, ctypes.c_int]
+        + [_dp] * 5 + [ctypes.c_int])
+    lib.oracle_heads_rows_fwd_bwd.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
     return lib
@@ -258,6 +264,34 @@ def head_fwd_tiled(q, k, v, scale, Br, Bc, causal=False, key_len=None, dropout_p
     if r != 0:
         raise ValueError("oracle_head_fwd_tiled rejected its arguments")
     return O, LSE
+
+
+def heads_rows_fwd_bwd(Qh, Kh, Vh, dOh, b_idx, h_idx, key_len, scale, row0, nrows,
+                       causal=False, dropout_p=0.0, seed=0, nthreads=0, _lib=None):
+    """Forward and backward of query rows [row0, row0+nrows) of selected heads.
+
+    Returns O_rows, LSE_rows, dQ_rows ([nh, nrows, ...]) and the rows'
+    contributions to dK and dV ([nh, N, d])."""
+    L = _lib or lib()
+    Qh, Kh, Vh, dOh = _f64(Qh), _f64(Kh), _f64(Vh), _f64(dOh)
+    nh, N, d = Qh.shape
+    b_idx = np.ascontiguousarray(b_idx, dtype=np.int32)
+    h_idx = np.ascontiguousarray(h_idx, dtype=np.int32)
+    key_len = np.ascontiguousarray(key_len, dtype=np.int32)
+    O = np.zeros((nh, nrows, d))
+    LSE = np.zeros((nh, nrows))
+    dQ = np.zeros((nh, nrows, d))
+    dK = np.zeros((nh, N, d))
+    dV = np.zeros((nh, N, d))
+    r = L.oracle_heads_rows_fwd_bwd(_ptr(Qh, _dp), _ptr(Kh, _dp), _ptr(Vh, _dp), _ptr(dOh, _dp),
+                                    nh, _ptr(b_idx, _ip), _ptr(h_idx, _ip), _ptr(key_len, _ip),
+                                    N, d, float(scale), int(bool(causal)), float(dropout_p),
+                                    int(seed), int(row0), int(nrows), _ptr(O, _dp),
+                                    _ptr(LSE, _dp), _ptr(dQ, _dp), _ptr(dK, _dp), _ptr(dV, _dp),
+                                    int(nthreads))
+    if r != 0:
+        raise ValueError("oracle_heads_rows_fwd_bwd rejected its arguments")
+    return O, LSE, dQ, dK, dV
 
 
 def num_threads() -> int:

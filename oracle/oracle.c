@@ -190,12 +190,13 @@ int oracle_head_fwd(const double* q, const double* k, const double* v, double* o
     if (!P || !F) { free(P); free(F); return -2; }
     scores_and_probs(q, k, N, d, scale, causal, key_len, P, lse);
     dropout_factors(N, p, seed, b, h, F);
+    /* O_i = sum_j P_ij F_ij V_j, accumulated key by key (row-major access). */
+    for (size_t x = 0; x < (size_t)N * d; ++x) o[x] = 0.0;
     for (int i = 0; i < N; ++i) {
-        for (int c = 0; c < d; ++c) {
-            double acc = 0.0;
-            for (int j = 0; j < N; ++j)
-                acc += P[(size_t)i * N + j] * F[(size_t)i * N + j] * v[(size_t)j * d + c];
-            o[(size_t)i * d + c] = acc;
+        for (int j = 0; j < N; ++j) {
+            double w = P[(size_t)i * N + j] * F[(size_t)i * N + j];
+            if (w == 0.0) continue;
+            for (int c = 0; c < d; ++c) o[(size_t)i * d + c] += w * v[(size_t)j * d + c];
         }
     }
     free(P); free(F);
@@ -225,21 +226,23 @@ int oracle_head_bwd(const double* q, const double* k, const double* v, const dou
     scores_and_probs(q, k, N, d, scale, causal, key_len, P, lse);
     dropout_factors(N, p, seed, b, h, F);
 
-    /* dV */
-    for (int j = 0; j < N; ++j)
-        for (int c = 0; c < d; ++c) {
-            double acc = 0.0;
-            for (int i = 0; i < N; ++i)
-                acc += P[(size_t)i * N + j] * F[(size_t)i * N + j] * dout[(size_t)i * d + c];
-            dv[(size_t)j * d + c] = acc;
+    /* dV_j = sum_i P_ij F_ij dO_i, accumulated query by query */
+    for (size_t x = 0; x < (size_t)N * d; ++x) dv[x] = 0.0;
+    for (int i = 0; i < N; ++i)
+        for (int j = 0; j < N; ++j) {
+            double w = P[(size_t)i * N + j] * F[(size_t)i * N + j];
+            if (w == 0.0) continue;
+            for (int c = 0; c < d; ++c) dv[(size_t)j * d + c] += w * dout[(size_t)i * d + c];
         }
     /* dP, D, dS */
     for (int i = 0; i < N; ++i) {
         double Di = 0.0;
         for (int j = 0; j < N; ++j) {
             double dp = 0.0;
-            for (int c = 0; c < d; ++c) dp += dout[(size_t)i * d + c] * v[(size_t)j * d + c];
-            dp *= F[(size_t)i * N + j];
+            if (P[(size_t)i * N + j] != 0.0) { /* dP_ij only enters through P_ij dP_ij */
+                for (int c = 0; c < d; ++c) dp += dout[(size_t)i * d + c] * v[(size_t)j * d + c];
+                dp *= F[(size_t)i * N + j];
+            }
             dS[(size_t)i * N + j] = dp; /* holds dP for now */
             Di += P[(size_t)i * N + j] * dp;
         }
@@ -254,13 +257,15 @@ int oracle_head_bwd(const double* q, const double* k, const double* v, const dou
             for (int j = 0; j < N; ++j) acc += dS[(size_t)i * N + j] * k[(size_t)j * d + c];
             dq[(size_t)i * d + c] = scale * acc;
         }
-    /* dK */
-    for (int j = 0; j < N; ++j)
-        for (int c = 0; c < d; ++c) {
-            double acc = 0.0;
-            for (int i = 0; i < N; ++i) acc += dS[(size_t)i * N + j] * q[(size_t)i * d + c];
-            dk[(size_t)j * d + c] = scale * acc;
+    /* dK_j = scale sum_i dS_ij Q_i, accumulated query by query */
+    for (size_t x = 0; x < (size_t)N * d; ++x) dk[x] = 0.0;
+    for (int i = 0; i < N; ++i)
+        for (int j = 0; j < N; ++j) {
+            double w = dS[(size_t)i * N + j];
+            if (w == 0.0) continue;
+            for (int c = 0; c < d; ++c) dk[(size_t)j * d + c] += w * q[(size_t)i * d + c];
         }
+    for (size_t x = 0; x < (size_t)N * d; ++x) dk[x] *= scale;
     free(P); free(F); free(dS); free(lse);
     return 0;
 }
@@ -314,6 +319,91 @@ int oracle_head_fwd_rows(const double* q, const double* k, const double* v,
     free(s);
     return 0;
 }
+
+/*
+ * Forward and backward of the query rows [row0, row0 + nrows) of one head,
+ * row by row, without an N x N array: O, LSE and dQ of those rows, and the
+ * rows' contributions to dK and dV added into dk_part and dv_part ([N][d],
+ * zeroed by the caller).  The same definitions as oracle_head_fwd and
+ * oracle_head_bwd, restricted to a slice of the rows; summed over a partition
+ * of all rows, the contributions give the head's dK and dV.
+ */
+int oracle_head_rows_fwd_bwd(const double* q, const double* k, const double* v,
+                             const double* dout, int row0, int nrows, double* o_rows,
+                             double* lse_rows, double* dq_rows, double* dk_part, double* dv_part,
+                             int N, int d, double scale, int causal, int key_len, double p,
+                             uint64_t seed, int b, int h) {
+    if (check_args(N, d, p, key_len) || row0 < 0 || nrows < 0 || row0 + nrows > N) return -1;
+    double* P = (double*)malloc(sizeof(double) * (size_t)N);
+    double* F = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!P || !F) { free(P); free(F); return -2; }
+    uint32_t t = oracle_dropout_threshold(p);
+    double inv = 1.0 / (1.0 - p);
+    for (int r = 0; r < nrows; ++r) {
+        const int i = row0 + r;
+        const double* qi = q + (size_t)i * d;
+        const double* gi = dout + (size_t)i * d;
+        double* oi = o_rows + (size_t)r * d;
+        double* dqi = dq_rows + (size_t)r * d;
+        for (int c = 0; c < d; ++c) { oi[c] = 0.0; dqi[c] = 0.0; }
+        double m = -INFINITY;
+        for (int j = 0; j < N; ++j) {
+            double sc = -INFINITY;
+            if (valid_pair(i, j, causal, key_len)) {
+                double acc = 0.0;
+                for (int c = 0; c < d; ++c) acc += qi[c] * k[(size_t)j * d + c];
+                sc = scale * acc;
+            }
+            P[j] = sc;
+            if (sc > m) m = sc;
+        }
+        if (m == -INFINITY) { lse_rows[r] = -INFINITY; continue; }
+        double l = 0.0;
+        for (int j = 0; j < N; ++j) {
+            P[j] = (P[j] == -INFINITY) ? 0.0 : exp(P[j] - m);
+            l += P[j];
+        }
+        for (int j = 0; j < N; ++j) {
+            P[j] /= l;
+            F[j] = 1.0;
+            if (p > 0.0) F[j] = oracle_dropout_keep(seed, b, h, i, j, t) ? inv : 0.0;
+        }
+        lse_rows[r] = m + log(l);
+        for (int j = 0; j < N; ++j) {          /* O_i */
+            double w = P[j] * F[j];
+            if (w == 0.0) continue;
+            for (int c = 0; c < d; ++c) oi[c] += w * v[(size_t)j * d + c];
+        }
+        double Di = 0.0;                        /* D_i = dO_i . O_i */
+        for (int c = 0; c < d; ++c) Di += gi[c] * oi[c];
+        for (int j = 0; j < N; ++j) {
+            if (P[j] == 0.0) continue;
+            double dp = 0.0;
+            for (int c = 0; c < d; ++c) dp += gi[c] * v[(size_t)j * d + c];
+            dp *= F[j];
+            const double ds = P[j] * (dp - Di);
+            const double w = P[j] * F[j];
+            for (int c = 0; c < d; ++c) {
+                dqi[c] += ds * k[(size_t)j * d + c];
+                dk_part[(size_t)j * d + c] += scale * ds * qi[c];
+                dv_part[(size_t)j * d + c] += w * gi[c];
+            }
+        }
+        for (int c = 0; c < d; ++c) dqi[c] *= scale;
+    }
+    free(P); free(F);
+    return 0;
+}
+
+/* Rows [row0, row0 + nrows) of nh heads (OpenMP over heads); array layout as in
+ * oracle_heads_fwd, with *_rows arrays [nh][nrows](...) and the partial dK,
+ * dV arrays [nh][N][d] (zeroed here). */
+int oracle_heads_rows_fwd_bwd(const double* Q, const double* K, const double* V,
+                              const double* dO, int nh, const int32_t* b_idx,
+                              const int32_t* h_idx, const int32_t* key_len, int N, int d,
+                              double scale, int causal, double p, uint64_t seed, int row0,
+                              int nrows, double* O_rows, double* LSE_rows, double* dQ_rows,
+                              double* dK_part, double* dV_part, int nthreads);
 
 /*
  * Tiled forward of one head following the online-softmax recurrence of
@@ -438,6 +528,28 @@ int oracle_heads_bwd(const double* Q, const double* K, const double* V, const do
                                 dQ + x * hd, dK + x * hd, dV + x * hd,
                                 D ? D + (size_t)x * N : NULL,
                                 N, d, scale, causal, key_len[x], p, seed, b_idx[x], h_idx[x]);
+        if (r) err |= 1;
+    }
+    return err ? -1 : 0;
+}
+
+int oracle_heads_rows_fwd_bwd(const double* Q, const double* K, const double* V,
+                              const double* dO, int nh, const int32_t* b_idx,
+                              const int32_t* h_idx, const int32_t* key_len, int N, int d,
+                              double scale, int causal, double p, uint64_t seed, int row0,
+                              int nrows, double* O_rows, double* LSE_rows, double* dQ_rows,
+                              double* dK_part, double* dV_part, int nthreads) {
+    if (nh < 0) return -1;
+    set_threads(nthreads);
+    int err = 0;
+    size_t hd = (size_t)N * d, rd = (size_t)nrows * d;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int x = 0; x < nh; ++x) {
+        for (size_t y = 0; y < hd; ++y) { dK_part[x * hd + y] = 0.0; dV_part[x * hd + y] = 0.0; }
+        int r = oracle_head_rows_fwd_bwd(Q + x * hd, K + x * hd, V + x * hd, dO + x * hd, row0,
+                                         nrows, O_rows + x * rd, LSE_rows + (size_t)x * nrows,
+                                         dQ_rows + x * rd, dK_part + x * hd, dV_part + x * hd, N, d,
+                                         scale, causal, key_len[x], p, seed, b_idx[x], h_idx[x]);
         if (r) err |= 1;
     }
     return err ? -1 : 0;

@@ -350,6 +350,29 @@ def pin_dropout_counter_layout(L) -> float:
     return float(bad)
 
 
+def pin_row_slices_partition(L) -> float:
+    """Row slices: O, LSE, dQ of each slice equal the full evaluation's rows,
+    and the slices' dK/dV contributions sum to the full dK/dV."""
+    N, d = 29, 8
+    worst = 0.0
+    for causal, key_len, p in ((False, 29, 0.0), (True, 21, 0.3)):
+        q, k, v, do = (_rand(1, 1, N, d) for _ in range(4))
+        O, LSE = oracle.attn_fwd(q, k, v, 0.4, causal, [key_len], p, 9, _lib=L)
+        dQ, dK, dV, _ = oracle.attn_bwd(q, k, v, do, 0.4, causal, [key_len], p, 9, _lib=L)
+        sk, sv = np.zeros((N, d)), np.zeros((N, d))
+        for r0, nr in ((0, 10), (10, 1), (11, 18)):
+            Or, Lr, dQr, dKp, dVp = oracle.heads_rows_fwd_bwd(
+                q[0], k[0], v[0], do[0], [0], [0], [key_len], 0.4, r0, nr, causal, p, 9, _lib=L)
+            sk += dKp[0]
+            sv += dVp[0]
+            worst = max(worst, np.abs(Or[0] - O[0, 0, r0:r0 + nr]).max(),
+                        np.abs(dQr[0] - dQ[0, 0, r0:r0 + nr]).max())
+            fin = np.isfinite(LSE[0, 0, r0:r0 + nr])
+            worst = max(worst, np.abs(Lr[0][fin] - LSE[0, 0, r0:r0 + nr][fin]).max())
+        worst = max(worst, np.abs(sk - dK[0, 0]).max(), np.abs(sv - dV[0, 0]).max())
+    return worst
+
+
 PINS = {
     "zero_query": (pin_zero_query, 1e-12),
     "causal_row0": (pin_causal_row0, 1e-12),
@@ -363,6 +386,7 @@ PINS = {
     "D_equals_dO_dot_O": (pin_D_equals_dO_dot_O, 1e-12),
     "tile_invariance": (pin_tile_invariance, 1e-12),
     "rows_variant": (pin_rows_variant, 1e-12),
+    "row_slices_partition": (pin_row_slices_partition, 1e-12),
     "dropout_statistics": (pin_dropout_statistics, 5.0),
     "dropout_threshold": (pin_dropout_threshold, 0.5),
     "dropout_counter_layout": (pin_dropout_counter_layout, 0.5),

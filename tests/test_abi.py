@@ -1,0 +1,131 @@
+"""The C ABI library loads, exports what include/gbattn.h declares, and rejects
+bad arguments before touching the GPU (CPU only: every call here returns
+before any CUDA call, so fake pointers are safe)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_58_gb300 as ea
+from exact_attention_58_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gbattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(ea.LIB_PATH):
+        _build.build()
+    return ea.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_status_string",
+                     "attn_version"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libgbattn.so does not export {name}"
+    # and nothing in the shared object is a C++-only stand-in
+    assert lib.attn_version() == 100
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert ea.attn_status_string(code) != "unknown status"
+    assert ea.attn_status_string(99) == "unknown status"
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every case fails validation first
+
+
+def _fwd(lib, **kw):
+    a = dict(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, LSE=FAKE, B=1, H=1, N=128, d=64, dtype=0,
+             scale=0.125, causal=0, key_lens=None, p=0.0, seed=0, dev_status=None, stream=None)
+    a.update(kw)
+    return lib.attn_fwd(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["H"], a["N"],
+                        a["d"], a["dtype"], a["scale"], a["causal"], a["key_lens"], a["p"],
+                        a["seed"], a["dev_status"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(Q=None), 1),
+    (dict(LSE=None), 1),
+    (dict(N=0), 1),
+    (dict(B=-1), 1),
+    (dict(d=96), 2),
+    (dict(d=256), 2),
+    (dict(dtype=1, d=128), 2),
+    (dict(dtype=7), 1),
+    (dict(scale=0.0), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(scale=-1.0), 1),
+    (dict(p=1.0), 1),
+    (dict(p=-0.1), 1),
+    (dict(K=FAKE + 8), 3),
+    (dict(O=FAKE + 2), 3),
+    (dict(B=65536, H=65536), 2),
+])
+def test_fwd_validation(lib, kw, expected):
+    assert _fwd(lib, **kw) == expected
+
+
+def _bwd(lib, **kw):
+    a = dict(B=1, H=1, N=128, d=64, dtype=0, scale=0.125, p=0.0, ws=FAKE, ws_bytes=1 << 20,
+             ptrs=[FAKE] * 9)
+    a.update(kw)
+    return lib.attn_bwd(*a["ptrs"], a["B"], a["H"], a["N"], a["d"], a["dtype"], a["scale"], 0,
+                        None, a["p"], 0, a["ws"], a["ws_bytes"], None, None)
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(ptrs=[FAKE] * 8 + [None]), 1),
+    (dict(dtype=1), 2),
+    (dict(d=80), 2),
+    (dict(ws=None), 4),
+    (dict(ws_bytes=16), 4),
+    (dict(ws=FAKE + 4), 3),
+    (dict(ptrs=[FAKE] * 5 + [FAKE + 4] + [FAKE] * 3), 3),
+    (dict(p=1.5), 1),
+])
+def test_bwd_validation(lib, kw, expected):
+    assert _bwd(lib, **kw) == expected
+
+
+def test_workspace_size(lib):
+    # D and log-sum-exp (2 floats per padded row) plus the fp32 dQ accumulator
+    assert ea.attn_bwd_workspace_size(2, 3, 130, 64) == 2 * 3 * 256 * (2 + 64) * 4
+    assert ea.attn_bwd_workspace_size(1, 1, 128, 128) == 128 * 130 * 4
+    assert ea.attn_bwd_workspace_size(1, 1, 128, 96) == 0
+
+
+def test_product_path_fails_loudly_without_the_library(tmp_path, monkeypatch):
+    """The binding has no fallback: a missing library is an error, not a CPU path."""
+    import importlib
+    monkeypatch.setattr(ea, "_lib", None)
+    monkeypatch.setattr(ea, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        ea.library()
+    monkeypatch.setattr(ea, "_lib", None)
+    importlib.reload(ea)
+
+
+def test_product_code_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "exact_attention_58_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "liboracle" not in text and "oracle.c" not in text, f

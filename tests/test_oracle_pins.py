@@ -50,10 +50,11 @@ def test_rejects_bad_arguments():
 # ---------------------------------------------------------------------------
 MUTATIONS = {
     "drop_D_term": ("* (dS[(size_t)i * N + j] - Di);", "* (dS[(size_t)i * N + j]);"),
-    "dK_sign": ("dk[(size_t)j * d + c] = scale * acc;", "dk[(size_t)j * d + c] = -scale * acc;"),
+    "dK_sign": ("for (size_t x = 0; x < (size_t)N * d; ++x) dk[x] *= scale;",
+                "for (size_t x = 0; x < (size_t)N * d; ++x) dk[x] *= -scale;"),
     "dQ_missing_scale": ("dq[(size_t)i * d + c] = scale * acc;", "dq[(size_t)i * d + c] = acc;"),
-    "dV_transposed_P": ("acc += P[(size_t)i * N + j] * F[(size_t)i * N + j] * dout[(size_t)i * d + c];",
-                        "acc += P[(size_t)j * N + i] * F[(size_t)i * N + j] * dout[(size_t)i * d + c];"),
+    "dV_transposed": ("dv[(size_t)j * d + c] += w * dout[(size_t)i * d + c];",
+                      "dv[(size_t)i * d + c] += w * dout[(size_t)j * d + c];"),
     "causal_off_by_one": ("if (causal && j > i) return 0;", "if (causal && j >= i) return 0;"),
     "scores_unscaled": ("                s = scale * acc;\n", "                s = acc;\n"),
     "dropout_no_rescale": ("oracle_dropout_keep(seed, b, h, i, j, t) ? inv : 0.0;",
