@@ -183,7 +183,8 @@ def oracle_sample(inp, w: Workload, heads: int, row0: int, nrows: int, threads: 
 
 
 def calibrate_rows(inp, w, heads, threads, target_s):
-    """Rows per head so that one oracle sample takes about target_s seconds."""
+    """Rows per head (around N/2) so that one oracle sample of `heads` heads
+    takes about target_s seconds."""
     row0 = w.N // 2
     oracle_sample(inp, w, heads, row0, 4, threads)           # warm: threads, pages
     probe = 32
@@ -193,15 +194,18 @@ def calibrate_rows(inp, w, heads, threads, target_s):
 
 
 def cpu_baseline(inp, w, target_s=15.0):
+    """The oracle on whole heads (all query rows), one head per core, as many
+    rounds of `cores` heads as fit in about target_s seconds."""
     threads = host_cores()
     heads = min(threads, w.B * w.H)
-    rows = calibrate_rows(inp, w, heads, threads, target_s)
-    row0 = max(0, w.N // 2 - rows // 2)
-    dt, flops = oracle_sample(inp, w, heads, row0, rows, threads)
+    dt1, fl1 = oracle_sample(inp, w, heads, 0, w.N, threads)   # one round, also a warm-up
+    rounds = max(1, min((w.B * w.H) // heads, int(target_s / max(dt1, 1e-3))))
+    nh = heads * rounds
+    dt, flops = oracle_sample(inp, w, nh, 0, w.N, threads)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"float64 oracle forward+backward of query rows [{row0}, {row0 + rows}) "
-                      f"of {heads} heads of {w.name}, one head per core, {dt:.1f} s; FLOPs "
-                      f"counted as 14 d per attended (query, key) pair"}
+            "sample": f"float64 oracle forward+backward of all {w.N} query rows of {nh} of the "
+                      f"{w.B * w.H} heads of {w.name} ({threads} threads, OpenMP over heads), "
+                      f"{dt:.1f} s; FLOPs counted as 14 d per attended (query, key) pair"}
 
 
 # ---------------------------------------------------------------------------

@@ -120,6 +120,7 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
         !make_tmap_bhnd(&tv, V, fp32, B * H, N, d))
         return ATTN_ERR_CUDA;
     FwdParams p{};
+    p.V = V;
     p.O = O;
     p.LSE = LSE;
     p.key_lens = key_lens;

@@ -102,21 +102,26 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(__nv_bfloat16* __re
 //   dV_j += (P Z/(1-p))^T dO_i,   dK_j += dS^T Q_i       (P, dS read from TMEM)
 // dK_j (times scale) and dV_j leave the chip once, at the end.
 //
-// Warp roles (320 threads):
-//   warps 0-3  compute: one thread per key row (TMEM lane), builds P and dS
-//   warps 4-7  dQ: one thread per query row, reads dQ from TMEM, adds it
+// Warp roles (448 threads):
+//   warps 0-3  compute, query columns 0-63 of the block: one thread per key
+//              row (TMEM lane) builds P and dS
+//   warps 4-7  compute, query columns 64-127
+//   warps 8-11 dQ: one thread per query row, reads dQ from TMEM and adds it
 //              into the workspace with vector atomics
-//   warp  8    TMA producer: K_j, V_j once; Q_i, dO_i, LSE_i, D_i per block
-//   warp  9    MMA issuer
+//   warp  12   TMA producer: K_j, V_j once; Q_i, dO_i, LSE_i, D_i per block
+//   warp  13   MMA issuer; dV/dK for query columns 0-63 start as soon as the
+//              first compute warpgroup is done
 //
 // Tensor memory (512 columns):
 //   d = 64:  dK [0,64) dV [64,128) S [128,256) dP [256,384) dQ [384,448)
-//   d = 128: dK [0,128) dV [128,256) S [256,384) dP [384,512); P and dS
-//            (bf16 pairs) take the first 64 columns of S and dP, and the two
-//            64-column halves of dQ go in their last 64 columns, so the next
-//            S^T waits until the dQ warps have read dQ out.
+//   d = 128: dK [0,128) dV [128,256) S [256,384) dP [384,512).  Each compute
+//            warpgroup writes its P and dS (bf16 pairs) into the first 32
+//            columns of its 64-column half of S and dP; dQ's four 32-column
+//            pieces go in the remaining 32-column gaps, so the next S^T waits
+//            until the dQ warps have read dQ out.
 template <int D>
 struct BwdCfg {
+    static constexpr int THREADS = 448;
     static constexpr int ROWB = D * 2;
     static constexpr int NCB = ROWB / 128;
     static constexpr int TILE = kTileRows * ROWB;
@@ -137,14 +142,19 @@ struct BwdCfg {
     static constexpr uint32_t C_S = 2 * D;
     static constexpr uint32_t C_DP = 2 * D + 128;
     static constexpr uint32_t C_DQ = 2 * D + 256;   // d = 64 only
+    static constexpr int DQ_N = (D == 64) ? 64 : 32;  // N of one dQ MMA
     static constexpr uint32_t IDESC_SDP = idesc_f32acc(128, 128, false, false, false);
     static constexpr uint32_t IDESC_DKV = idesc_f32acc(128, D, false, false, true);
-    static constexpr uint32_t IDESC_DQ = idesc_f32acc(128, 64, false, true, true);
+    static constexpr uint32_t IDESC_DQ = idesc_f32acc(128, DQ_N, false, true, true);
     static_assert(SMEM <= 232448, "shared memory budget");
+    // TMEM column of dQ columns [32 q, 32 q + 32) when d = 128
+    __device__ static constexpr uint32_t dq_col128(int q) {
+        return (q < 2 ? C_S : C_DP) + ((q & 1) ? 96u : 32u);
+    }
 };
 
 template <int D, bool kCausal, bool kDropout>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV,
@@ -155,14 +165,8 @@ __global__ void __launch_bounds__(320, 1)
     const int lane = threadIdx.x & 31;
 
     const int BH = p.B * p.H;
-    int kb, bh;
-    if (kCausal) {   // key block 0 meets every query block: heaviest first
-        kb = static_cast<int>(blockIdx.x) / BH;
-        bh = static_cast<int>(blockIdx.x) % BH;
-    } else {
-        kb = static_cast<int>(blockIdx.x) % p.nkb;
-        bh = static_cast<int>(blockIdx.x) / p.nkb;
-    }
+    int kb, bh;   // causal: key block 0 meets every query block, so rank 0 is heaviest
+    grouped_schedule(static_cast<int>(blockIdx.x), BH, p.nkb, bh, kb);
     const int b = bh / p.H, h = bh % p.H;
     const int N = p.N;
     int L = N;
@@ -200,12 +204,12 @@ __global__ void __launch_bounds__(320, 1)
     uint64_t* full_q = bars + 1;      // [2]
     uint64_t* empty_q = bars + 3;     // [2]
     uint64_t* bar_S = bars + 5;
-    uint64_t* bar_P = bars + 6;
-    uint64_t* bar_dQ = bars + 7;
-    uint64_t* bar_dQfree = bars + 8;
-    uint64_t* bar_dkdv = bars + 9;
-    uint64_t* bar_fin = bars + 10;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 11);
+    uint64_t* bar_P = bars + 6;       // [2] one per compute warpgroup
+    uint64_t* bar_dQ = bars + 8;
+    uint64_t* bar_dQfree = bars + 9;
+    uint64_t* bar_dkdv = bars + 10;
+    uint64_t* bar_fin = bars + 11;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 12);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
     float* sLSE = reinterpret_cast<float*>(smem + C::OFF_LSE);
     float* sD = reinterpret_cast<float*>(smem + C::OFF_D);
@@ -215,9 +219,9 @@ __global__ void __launch_bounds__(320, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&full_q[s], 1);
             mbar_init(&empty_q[s], 1);
+            mbar_init(&bar_P[s], kTileRows);
         }
         mbar_init(bar_S, 1);
-        mbar_init(bar_P, kTileRows);
         mbar_init(bar_dQ, 1);
         mbar_init(bar_dQfree, kTileRows);
         mbar_init(bar_dkdv, 1);
@@ -225,7 +229,7 @@ __global__ void __launch_bounds__(320, 1)
         *s_abort = 0;
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == 13) {
         tmem_alloc(s_tmem, 512);
         tmem_relinquish();
     }
@@ -234,7 +238,7 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    if (warp == 8) {
+    if (warp == 12) {
         // ================= TMA producer =================
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
@@ -272,12 +276,25 @@ __global__ void __launch_bounds__(320, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 9) {
+    } else if (warp == 13) {
         // ================= MMA issuer =================
         if (lane == 0) {
             const uint32_t sK = smem_u32(smem + C::OFF_K);
             const uint32_t sV = smem_u32(smem + C::OFF_V);
             const uint32_t sdS = smem_u32(smem + C::OFF_DS);
+            // dV += P^T dO and dK += dS^T Q over query columns [64 hh, 64 hh + 64)
+            auto issue_dkv_half = [&](int hh, uint32_t sQ, uint32_t sdO, bool first) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ts<false>(tmem + C::C_DV, tmem + C::C_S + 64 * hh + 8 * kk,
+                                  sdesc_sw128(sdO + (4 * hh + kk) * 2048, C::CB_BYTES, 1024),
+                                  C::IDESC_DKV, (first && kk == 0) ? 0u : 1u);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ts<false>(tmem + C::C_DK, tmem + C::C_DP + 64 * hh + 8 * kk,
+                                  sdesc_sw128(sQ + (4 * hh + kk) * 2048, C::CB_BYTES, 1024),
+                                  C::IDESC_DKV, (first && kk == 0) ? 0u : 1u);
+            };
             bool ok = mbar_wait(bar_kv, 0, s_abort);
             for (int it = 0; it < nq && ok; ++it) {
                 const int stage = it & 1;
@@ -301,7 +318,11 @@ __global__ void __launch_bounds__(320, 1)
                                   sdesc_sw128(sdO + off, 16, 1024), C::IDESC_SDP, kk > 0);
                 }
                 tc_commit(bar_S);
-                ok = mbar_wait(bar_P, it & 1, s_abort);
+                ok = mbar_wait(&bar_P[0], it & 1, s_abort);
+                if (!ok) break;
+                tc_fence_after();
+                issue_dkv_half(0, sQ, sdO, it == 0);
+                ok = mbar_wait(&bar_P[1], it & 1, s_abort);
                 if (ok && D == 64 && it > 0) ok = mbar_wait(bar_dQfree, (it - 1) & 1, s_abort);
                 if (!ok) break;
                 tc_fence_after();
@@ -312,25 +333,16 @@ __global__ void __launch_bounds__(320, 1)
                         mma_ss<false>(tmem + C::C_DQ, ad, sdesc_sw128(sK + kk * 2048, C::CB_BYTES, 1024),
                                       C::IDESC_DQ, kk > 0);
                     } else {
-                        mma_ss<false>(tmem + C::C_S + 64, ad,
-                                      sdesc_sw128(sK + kk * 2048, C::CB_BYTES, 1024), C::IDESC_DQ,
-                                      kk > 0);
-                        mma_ss<false>(tmem + C::C_DP + 64, ad,
-                                      sdesc_sw128(sK + C::CB_BYTES + kk * 2048, C::CB_BYTES, 1024),
-                                      C::IDESC_DQ, kk > 0);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            mma_ss<false>(tmem + C::dq_col128(q), ad,
+                                          sdesc_sw128(sK + (q >> 1) * C::CB_BYTES + (q & 1) * 64 + kk * 2048,
+                                                      C::CB_BYTES, 1024),
+                                          C::IDESC_DQ, kk > 0);
                     }
                 }
                 tc_commit(bar_dQ);
-#pragma unroll
-                for (int kk = 0; kk < kTileRows / 16; ++kk)   // dV += P^T dO  (K = queries)
-                    mma_ts<false>(tmem + C::C_DV, tmem + C::C_S + kk * 8,
-                                  sdesc_sw128(sdO + kk * 2048, C::CB_BYTES, 1024), C::IDESC_DKV,
-                                  (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < kTileRows / 16; ++kk)   // dK += dS^T Q
-                    mma_ts<false>(tmem + C::C_DK, tmem + C::C_DP + kk * 8,
-                                  sdesc_sw128(sQ + kk * 2048, C::CB_BYTES, 1024), C::IDESC_DKV,
-                                  (it > 0 || kk > 0) ? 1u : 0u);
+                issue_dkv_half(1, sQ, sdO, false);
                 tc_commit(&empty_q[stage]);
             }
             if (ok) tc_commit(bar_dkdv);
@@ -339,13 +351,17 @@ __global__ void __launch_bounds__(320, 1)
             mbar_wait(bar_fin, 0, &no_abort);
         }
         __syncwarp();
-    } else if (warp < 4) {
+    } else if (warp < 8) {
         // ================= compute: P and dS, one key row per thread =================
-        const int r = warp * 32 + lane;
+        const int hh = warp >> 2;          // query-column half of this warpgroup
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
         const int j = k0 + r;
-        const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const uint32_t tS = tl + C::C_S + 64 * hh;
+        const uint32_t tdP = tl + C::C_DP + 64 * hh;
         const bool row_valid = j < L;
-        uint8_t* sdS = smem + C::OFF_DS;
+        uint8_t* rowp = smem + C::OFF_DS + hh * C::CB_BYTES + r * 128;
         bool ok = true;
         for (int it = 0; it < nq; ++it) {
             const int stage = it & 1;
@@ -357,24 +373,35 @@ __global__ void __launch_bounds__(320, 1)
                 break;
             }
             tc_fence_after();
-            const float* lse_s = sLSE + stage * kTileRows;
-            const float* d_s = sD + stage * kTileRows;
+            const float* lse_s = sLSE + stage * kTileRows + 64 * hh;
+            const float* d_s = sD + stage * kTileRows + 64 * hh;
+            const int q0h = qi * kTileRows + 64 * hh;   // first query of this half
             const bool diag = kCausal && (qi == kb);
-#pragma unroll 1
+            // 16-column chunks; the next chunk's TMEM loads overlap this chunk's math.
+            uint32_t sbuf[2][16], dbuf[2][16];
+            tmem_ld16(tS, sbuf[0]);
+            tmem_ld16(tdP, dbuf[0]);
+            tmem_ld_wait();
+            reg_fence(sbuf[0]);
+            reg_fence(dbuf[0]);
+#pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t sv[32], dpv[32];
-                tmem_ld32(tl + C::C_S + 32 * c, sv);
-                tmem_ld32(tl + C::C_DP + 32 * c, dpv);
-                tmem_ld_wait();
-                reg_fence(sv);
-                reg_fence(dpv);
-                uint32_t keep = 0xFFFFFFFFu;   // bit e: column 32c+e kept
+                if (c < 3) {
+                    tmem_ld16(tS + 16 * (c + 1), sbuf[(c + 1) & 1]);
+                    tmem_ld16(tdP + 16 * (c + 1), dbuf[(c + 1) & 1]);
+                }
+                const uint32_t* sv = sbuf[c & 1];
+                const uint32_t* dpv = dbuf[c & 1];
+                uint32_t keep = 0xFFFFu;   // bit e: column 16c+e of this half kept
                 if constexpr (kDropout) {
+                    // Lanes 4m..4m+3 own keys 4m..4m+3 of one Philox counter
+                    // (i, j>>2, h, b): lane a draws the words of query 4g+a and
+                    // the quad swaps bits so each lane gets its own key's bits.
                     keep = 0u;
                     const int a = lane & 3;
 #pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        const int iq = qi * kTileRows + 32 * c + 4 * g + a;
+                    for (int g = 0; g < 4; ++g) {
+                        const int iq = q0h + 16 * c + 4 * g + a;
                         uint32_t v = dropout_keep4(p.seed_lo, p.seed_hi, p.drop_threshold, iq,
                                                    j & ~3, h, b)
                                      << (4 * a);
@@ -386,17 +413,16 @@ __global__ void __launch_bounds__(320, 1)
                             keep |= ((v >> (4 * a2 + e)) & 1u) << (4 * g + a2);
                     }
                 }
-                uint32_t pk[16], dk[16];
+                uint32_t pk[8], dk[8];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
+                for (int e = 0; e < 8; ++e) {
                     float pd[2], ds[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const int col = 32 * c + 2 * e + u;
-                        const int iq = qi * kTileRows + col;
+                        const int col = 16 * c + 2 * e + u;
                         float pr = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), p.scale_log2,
                                                    -lse_s[col]));
-                        const bool valid = row_valid && (!diag || j <= iq);
+                        const bool valid = row_valid && (!diag || j <= q0h + col);
                         pr = valid ? pr : 0.f;
                         float dp = __uint_as_float(dpv[2 * e + u]);
                         float pdrop = pr;
@@ -411,92 +437,96 @@ __global__ void __launch_bounds__(320, 1)
                     pk[e] = pack_bf16x2(pd[0], pd[1]);
                     dk[e] = pack_bf16x2(ds[0], ds[1]);
                 }
-                tmem_st16(tl + C::C_S + 16 * c, pk);
-                tmem_st16(tl + C::C_DP + 16 * c, dk);
+                tmem_st8(tS + 8 * c, pk);
+                tmem_st8(tdP + 8 * c, dk);
                 // dS (bf16) into shared memory as the dQ MMA's A operand: query
-                // index innermost (MN-major), 128-byte swizzle.
-                uint8_t* rowp = sdS + (c >> 1) * C::CB_BYTES + r * 128;
+                // index innermost (MN-major, one 64-query block per half), 128-byte
+                // swizzle.
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int chunk = ((c & 1) * 4 + u) ^ (r & 7);
+                for (int u = 0; u < 2; ++u) {
+                    const int chunk = (2 * c + u) ^ (r & 7);
                     *reinterpret_cast<uint4*>(rowp + chunk * 16) =
                         make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+                }
+                if (c < 3) {
+                    tmem_ld_wait();
+                    reg_fence(sbuf[(c + 1) & 1]);
+                    reg_fence(dbuf[(c + 1) & 1]);
                 }
             }
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bar_P);
+            mbar_arrive(&bar_P[hh]);
         }
-        // ---- epilogue: dK = scale * acc, dV = acc, to bf16 ----
+        // ---- epilogue: warpgroup 0 writes dK = scale * acc, warpgroup 1 dV ----
         if (ok) {
             ok = mbar_wait_warp(bar_dkdv, 0, s_abort);
             tc_fence_after();
         }
         if (ok) {
+            const uint32_t src = tl + (hh == 0 ? C::C_DK : C::C_DV);
+            const float mul = (hh == 0) ? p.scale : 1.f;
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(hh == 0 ? p.dK : p.dV);
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
-                uint32_t a[32], v[32];
-                tmem_ld32(tl + C::C_DK + 32 * c, a);
-                tmem_ld32(tl + C::C_DV + 32 * c, v);
+                uint32_t a[32];
+                tmem_ld32(src + 32 * c, a);
                 tmem_ld_wait();
                 reg_fence(a);
-                reg_fence(v);
                 if (j < N) {
-                    const size_t off = head_off + static_cast<size_t>(j) * D + 32 * c;
-                    uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dK) + off);
-                    uint4* dv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dV) + off);
+                    uint4* dst = reinterpret_cast<uint4*>(out + head_off + static_cast<size_t>(j) * D + 32 * c);
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t wk[4], wv[4];
+                        uint32_t w[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            wk[e] = pack_bf16x2(__uint_as_float(a[8 * q4 + 2 * e]) * p.scale,
-                                                __uint_as_float(a[8 * q4 + 2 * e + 1]) * p.scale);
-                            wv[e] = pack_bf16x2(__uint_as_float(v[8 * q4 + 2 * e]),
-                                                __uint_as_float(v[8 * q4 + 2 * e + 1]));
-                        }
-                        dk[q4] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
-                        dv[q4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = pack_bf16x2(__uint_as_float(a[8 * q4 + 2 * e]) * mul,
+                                               __uint_as_float(a[8 * q4 + 2 * e + 1]) * mul);
+                        dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
             }
         }
     } else {
         // ================= dQ: one query row per thread =================
-        const int rq = (warp - 4) * 32 + lane;
+        const int rq = (warp & 3) * 32 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         for (int it = 0; it < nq; ++it) {
             const int i = (q_begin + it) * kTileRows + rq;
             if (!mbar_wait_warp(bar_dQ, it & 1, s_abort)) break;
             tc_fence_after();
-            uint32_t x[D / 32][32];
-            if constexpr (D == 64) {
-                tmem_ld32(tl + C::C_DQ, x[0]);
-                tmem_ld32(tl + C::C_DQ + 32, x[1]);
-            } else {
-                tmem_ld32(tl + C::C_S + 64, x[0]);
-                tmem_ld32(tl + C::C_S + 96, x[1]);
-                tmem_ld32(tl + C::C_DP + 64, x[2]);
-                tmem_ld32(tl + C::C_DP + 96, x[3]);
-            }
-            tmem_ld_wait();
+            float4* dst = reinterpret_cast<float4*>(p.dq_acc + (static_cast<size_t>(bh) * p.Npad + i) * D);
+            // d = 64: one 64-column piece.  d = 128: pieces 0,1 then 2,3; the
+            // TMEM columns are released after the last load.
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) reg_fence(x[c]);
-            tc_fence_before();
-            mbar_arrive(bar_dQfree);
-            if (i < N) {
-                float4* dst = reinterpret_cast<float4*>(
-                    p.dq_acc + (static_cast<size_t>(bh) * p.Npad + i) * D);
+            for (int half = 0; half < D / 64; ++half) {
+                uint32_t x[2][32];
+                if constexpr (D == 64) {
+                    tmem_ld32(tl + C::C_DQ, x[0]);
+                    tmem_ld32(tl + C::C_DQ + 32, x[1]);
+                } else {
+                    tmem_ld32(tl + C::dq_col128(2 * half), x[0]);
+                    tmem_ld32(tl + C::dq_col128(2 * half + 1), x[1]);
+                }
+                tmem_ld_wait();
+                reg_fence(x[0]);
+                reg_fence(x[1]);
+                if (half == D / 64 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(bar_dQfree);
+                }
+                if (i < N) {
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c)
+                    for (int c = 0; c < 2; ++c)
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        atomicAdd(dst + c * 8 + v,
-                                  make_float4(__uint_as_float(x[c][4 * v]),
-                                              __uint_as_float(x[c][4 * v + 1]),
-                                              __uint_as_float(x[c][4 * v + 2]),
-                                              __uint_as_float(x[c][4 * v + 3])));
+                        for (int v = 0; v < 8; ++v)
+                            atomicAdd(dst + half * 16 + c * 8 + v,
+                                      make_float4(__uint_as_float(x[c][4 * v]),
+                                                  __uint_as_float(x[c][4 * v + 1]),
+                                                  __uint_as_float(x[c][4 * v + 2]),
+                                                  __uint_as_float(x[c][4 * v + 3])));
+                }
             }
         }
     }
@@ -504,7 +534,7 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 9) tmem_dealloc(tmem, 512);
+    if (warp == 13) tmem_dealloc(tmem, 512);
     if (threadIdx.x == 0 && *s_abort && p.dev_status != nullptr)
         atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_DEVICE_TIMEOUT));
 }
@@ -521,7 +551,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
         configured = true;
     }
     const unsigned grid = static_cast<unsigned>(p.nkb) * static_cast<unsigned>(p.B * p.H);
-    kern<<<grid, 320, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+    kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
     return cudaGetLastError();
 }
 

@@ -52,11 +52,38 @@ struct FwdCfg {
     static constexpr int PV_STEPS = kTileRows / KSTEP;     // MMAs per P V
     static constexpr int SMEM = (2 + NSLOT) * TILE + 1024 /*barriers*/ + 1024 /*align*/;
     static constexpr uint32_t IDESC_QK = idesc_f32acc(128, 128, kTF32, false, false);
-    static constexpr uint32_t IDESC_PV = idesc_f32acc(128, D, kTF32, false, true);
+    static constexpr uint32_t IDESC_PV = idesc_f32acc(128, D, kTF32, false, !kTF32);
     static_assert(ROWB == 128 || ROWB == 256, "tile rows must be 128 or 256 bytes");
 };
 
 constexpr uint32_t kTmemCols = 512;
+
+// fp32 V_j (keys k0..k0+127 of one head, [N][D] in global memory) written into
+// a shared-memory slot as the K-major B operand of O += P V: D rows (one per
+// head-dim column) of 128 keys, in 32-key column blocks of D x 128 bytes,
+// 128-byte swizzle.  Keys past N are written as zeros.  One warp.
+template <int D>
+__device__ __forceinline__ void store_v_transposed(const float* __restrict__ Vh, uint8_t* dst,
+                                                   int k0, int N, int lane) {
+#pragma unroll 1
+    for (int t = 0; t < 4; ++t) {
+        const int k = lane + 32 * t;       // key within the block; column block t
+        const int key = k0 + k;
+        const uint32_t kb_off = t * (D * 128) + (static_cast<uint32_t>(k & 3) << 2);
+#pragma unroll 4
+        for (int c4 = 0; c4 < D / 4; ++c4) {
+            const float4 v = (key < N) ? *reinterpret_cast<const float4*>(Vh + static_cast<size_t>(key) * D + 4 * c4)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c = 4 * c4 + e;
+                const uint32_t byte = kb_off + c * 128 + ((((k & 31) >> 2) ^ (c & 7)) << 4);
+                *reinterpret_cast<float*>(dst + byte) = vv[e];
+            }
+        }
+    }
+}
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -88,13 +115,8 @@ __global__ void __launch_bounds__(320, 1)
     // ---- which 256 query rows of which head ----
     const int BH = p.B * p.H;
     int qb, bh;
-    if (kCausal) {   // heaviest query blocks first
-        qb = p.nqb - 1 - static_cast<int>(blockIdx.x) / BH;
-        bh = static_cast<int>(blockIdx.x) % BH;
-    } else {         // neighbouring CTAs share a head's K/V in L2
-        qb = static_cast<int>(blockIdx.x) % p.nqb;
-        bh = static_cast<int>(blockIdx.x) / p.nqb;
-    }
+    grouped_schedule(static_cast<int>(blockIdx.x), BH, p.nqb, bh, qb);
+    if (kCausal) qb = p.nqb - 1 - qb;   // the last query blocks see the most keys
     const int b = bh / p.H, h = bh % p.H;
     const int N = p.N;
     int L = N;
@@ -148,40 +170,57 @@ __global__ void __launch_bounds__(320, 1)
 
     if (warp == 8) {
         // ================= TMA producer =================
-        if (lane == 0 && nkv > 0) {
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-            const int ntiles = (nkv_t[1] > 0) ? 2 : 1;
-            mbar_arrive_expect_tx(bar_q, ntiles * C::TILE);
-            for (int t = 0; t < ntiles; ++t)
-                for (int cb = 0; cb < C::NCB; ++cb)
-                    tma_load_3d(sQ + t * C::TILE + cb * C::CB_BYTES, &tmQ, bar_q, cb * C::BOXW,
-                                q0 + t * kTileRows, bh);
+        // The whole warp walks the ring (waits are warp-collective); lane 0
+        // issues the TMA copies.  TF32 products only take a K-major B, so for
+        // fp32 inputs the warp itself writes V_j transposed (keys along K)
+        // into its slot instead of a TMA copy.
+        if (nkv > 0) {
+            if (lane == 0) {
+                tma_prefetch_desc(&tmQ);
+                tma_prefetch_desc(&tmK);
+                tma_prefetch_desc(&tmV);
+                const int ntiles = (nkv_t[1] > 0) ? 2 : 1;
+                mbar_arrive_expect_tx(bar_q, ntiles * C::TILE);
+                for (int t = 0; t < ntiles; ++t)
+                    for (int cb = 0; cb < C::NCB; ++cb)
+                        tma_load_3d(sQ + t * C::TILE + cb * C::CB_BYTES, &tmQ, bar_q,
+                                    cb * C::BOXW, q0 + t * kTileRows, bh);
+            }
             int seq = 0;
             bool ok = true;
             for (int j = 0; j < nkv && ok; ++j) {
                 for (int which = 0; which < 2; ++which) {
                     const int slot = seq % C::NSLOT;
                     const uint32_t ph = (seq / C::NSLOT) & 1;
-                    if (!mbar_wait(&empty[slot], ph ^ 1, s_abort)) {
+                    if (!mbar_wait_warp(&empty[slot], ph ^ 1, s_abort)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[slot], C::TILE);
-                    const CUtensorMap* m = which ? &tmV : &tmK;
-                    for (int cb = 0; cb < C::NCB; ++cb)
-                        tma_load_3d(sKV + slot * C::TILE + cb * C::CB_BYTES, m, &full[slot],
-                                    cb * C::BOXW, j * kTileRows, bh);
+                    if (kTF32 && which == 1) {
+                        store_v_transposed<D>(static_cast<const float*>(p.V) +
+                                                  static_cast<size_t>(bh) * N * D,
+                                              sKV + slot * C::TILE, j * kTileRows, N, lane);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&full[slot]);
+                    } else if (lane == 0) {
+                        mbar_arrive_expect_tx(&full[slot], C::TILE);
+                        const CUtensorMap* m = which ? &tmV : &tmK;
+                        for (int cb = 0; cb < C::NCB; ++cb)
+                            tma_load_3d(sKV + slot * C::TILE + cb * C::CB_BYTES, m, &full[slot],
+                                        cb * C::BOXW, j * kTileRows, bh);
+                    }
                     ++seq;
                 }
             }
-            // Drain: every load this thread issued has landed before teardown.
-            volatile int no_abort = 0;
-            mbar_wait(bar_q, 0, &no_abort);
-            for (int s = 0; s < C::NSLOT && s < seq; ++s) {
-                const int uses = (seq - s + C::NSLOT - 1) / C::NSLOT;
-                mbar_wait(&full[s], (uses - 1) & 1, &no_abort);
+            // Drain: every load this warp issued has landed before teardown.
+            if (lane == 0) {
+                volatile int no_abort = 0;
+                mbar_wait(bar_q, 0, &no_abort);
+                for (int s = 0; s < C::NSLOT && s < seq; ++s) {
+                    const int uses = (seq - s + C::NSLOT - 1) / C::NSLOT;
+                    mbar_wait(&full[s], (uses - 1) & 1, &no_abort);
+                }
             }
         }
         __syncwarp();
@@ -205,8 +244,12 @@ __global__ void __launch_bounds__(320, 1)
                 const uint32_t a_tmem = tmem + 128u * t;
 #pragma unroll
                 for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-                    const uint64_t bd = sdesc_sw128(skv + slot * C::TILE + kk * C::KSTEP * 128,
-                                                    C::CB_BYTES, 1024);
+                    // bf16: V as stored (MN-major); fp32: V transposed (K-major)
+                    const uint64_t bd =
+                        kTF32 ? sdesc_sw128(skv + slot * C::TILE + (kk >> 2) * (D * 128) + (kk & 3) * 32,
+                                            16, 1024)
+                              : sdesc_sw128(skv + slot * C::TILE + kk * C::KSTEP * 128, C::CB_BYTES,
+                                            1024);
                     mma_ts<kTF32>(d_tmem, a_tmem + kk * 8, bd, C::IDESC_PV,
                                   (accumulate || kk > 0) ? 1u : 0u);
                 }
@@ -295,25 +338,36 @@ __global__ void __launch_bounds__(320, 1)
                 break;
             }
             tc_fence_after();
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(t_S + 32 * c, sr[c]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
-
             const int k0 = j * kTileRows;
             const bool tile_mask = (k0 + kTileRows > L) ||
                                    (kCausal && k0 + kTileRows - 1 > tile_first_row);
-            if (tile_mask) {
-                const int lim = (kCausal ? min(L, row + 1) : L) - k0;
+            // columns >= lim of this row are masked (only on masked tiles)
+            const int lim = tile_mask ? (kCausal ? min(L, row + 1) : L) - k0 : kTileRows;
+
+            // ---- pass 1: row max (S read from TMEM, eight independent chains) ----
+            float mx;
+            {
+                uint32_t sr[4][32];
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c >= lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+                for (int c = 0; c < 4; ++c) tmem_ld32(t_S + 32 * c, sr[c]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+                if (tile_mask) {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c >= lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+                }
+                float mp[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 128; c += 2)
+                    mp[(c >> 1) & 7] = max3f(mp[(c >> 1) & 7], __uint_as_float(sr[c >> 5][c & 31]),
+                                             __uint_as_float(sr[c >> 5][(c & 31) + 1]));
+                mx = max3f(max3f(mp[0], mp[1], mp[2]), max3f(mp[3], mp[4], mp[5]),
+                           fmaxf(mp[6], mp[7]));
             }
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
             const float m_new = fmaxf(m_ref, mx * p.scale_log2);
             const bool want = (m_ref != -INFINITY) && (m_new > m_ref + kRescaleThreshold);
             const bool warp_rescale = __any_sync(0xffffffffu, want);
@@ -326,26 +380,47 @@ __global__ void __launch_bounds__(320, 1)
             }
             const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
+            // ---- pass 2: P = exp2(s scale log2e - m), chunk by chunk (S re-read
+            // from TMEM, next chunk's load overlapping this chunk's math) ----
             float rowsum = 0.f;
-            if constexpr (!kTF32) {
+            const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+            const uint64_t nm2 = f2_pack(neg_m, neg_m);
+            uint64_t acc2[4];
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+            for (int k = 0; k < 4; ++k) acc2[k] = f2_pack(0.f, 0.f);
+            uint32_t buf[2][32];
+            tmem_ld32(t_S, buf[0]);
+            tmem_ld_wait();
+            reg_fence(buf[0]);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                if (cc < 3) tmem_ld32(t_S + 32 * (cc + 1), buf[(cc + 1) & 1]);
+                uint32_t* sv = buf[cc & 1];
+                if (tile_mask) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (32 * cc + e >= lim) sv[e] = __float_as_uint(-INFINITY);
+                }
+                if constexpr (!kTF32) {
+                    // exp2 arguments two at a time (paired FMA); the row sum adds
+                    // the bf16-rounded P in four independent paired chains.
                     uint32_t pk[16];
 #pragma unroll
                     for (int g = 0; g < 8; ++g) {   // 4 keys per group
-                        const int c = 32 * cc + 4 * g;
                         uint32_t keep = 0xFu;
                         if constexpr (kDropout)
                             keep = dropout_keep4(p.seed_lo, p.seed_hi, p.drop_threshold, row,
-                                                 k0 + c, h, b);
+                                                 k0 + 32 * cc + 4 * g, h, b);
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            const float x0 = ex2_approx(
-                                fmaf(__uint_as_float(sr[cc][4 * g + 2 * e]), p.scale_log2, neg_m));
-                            const float x1 = ex2_approx(fmaf(
-                                __uint_as_float(sr[cc][4 * g + 2 * e + 1]), p.scale_log2, neg_m));
-                            uint32_t u = pack_bf16x2(x0, x1);
-                            rowsum += bf16lo_to_f32(u) + bf16hi_to_f32(u);
+                            float x0, x1;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[4 * g + 2 * e]),
+                                                     __uint_as_float(sv[4 * g + 2 * e + 1])),
+                                             sc2, nm2),
+                                      x0, x1);
+                            uint32_t u = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+                            acc2[(2 * g + e) & 3] = f2_add(
+                                acc2[(2 * g + e) & 3], f2_pack(bf16lo_to_f32(u), bf16hi_to_f32(u)));
                             if constexpr (kDropout) {
                                 const uint32_t km = ((keep >> (2 * e)) & 1u ? 0x0000FFFFu : 0u) |
                                                     ((keep >> (2 * e + 1)) & 1u ? 0xFFFF0000u : 0u);
@@ -355,28 +430,41 @@ __global__ void __launch_bounds__(320, 1)
                         }
                     }
                     tmem_st16(t_S + 16 * cc, pk);
-                }
-            } else {
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                } else {
                     uint32_t pf[32];
 #pragma unroll
                     for (int g = 0; g < 8; ++g) {
-                        const int c = 32 * cc + 4 * g;
                         uint32_t keep = 0xFu;
                         if constexpr (kDropout)
                             keep = dropout_keep4(p.seed_lo, p.seed_hi, p.drop_threshold, row,
-                                                 k0 + c, h, b);
+                                                 k0 + 32 * cc + 4 * g, h, b);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float x = ex2_approx(
-                                fmaf(__uint_as_float(sr[cc][4 * g + e]), p.scale_log2, neg_m));
-                            rowsum += x;
-                            pf[4 * g + e] = ((keep >> e) & 1u) ? __float_as_uint(x) : 0u;
+                        for (int e = 0; e < 2; ++e) {
+                            float x0, x1;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[4 * g + 2 * e]),
+                                                     __uint_as_float(sv[4 * g + 2 * e + 1])),
+                                             sc2, nm2),
+                                      x0, x1);
+                            x0 = ex2_approx(x0);
+                            x1 = ex2_approx(x1);
+                            acc2[(2 * g + e) & 3] = f2_add(acc2[(2 * g + e) & 3], f2_pack(x0, x1));
+                            pf[4 * g + 2 * e] = ((keep >> (2 * e)) & 1u) ? __float_as_uint(x0) : 0u;
+                            pf[4 * g + 2 * e + 1] =
+                                ((keep >> (2 * e + 1)) & 1u) ? __float_as_uint(x1) : 0u;
                         }
                     }
                     tmem_st32(t_S + 32 * cc, pf);
                 }
+                if (cc < 3) {
+                    tmem_ld_wait();
+                    reg_fence(buf[(cc + 1) & 1]);
+                }
+            }
+            {
+                float a0, a1, a2, a3;
+                f2_unpack(f2_add(acc2[0], acc2[1]), a0, a1);
+                f2_unpack(f2_add(acc2[2], acc2[3]), a2, a3);
+                rowsum = (a0 + a1) + (a2 + a3);
             }
             l = l * alpha + rowsum;
             if (warp_rescale && j > 0) {   // O row *= alpha (PV of block j-1 is complete)

@@ -14,6 +14,7 @@ constexpr int kTileRows = 128;
 constexpr int kFwdRowsPerCta = 2 * kTileRows;
 
 struct FwdParams {
+    const void* V;            // read directly (not through TMA) on the fp32 path
     void* O;
     float* LSE;
     const int32_t* key_lens;
