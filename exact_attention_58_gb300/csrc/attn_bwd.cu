@@ -99,26 +99,31 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(__nv_bfloat16* __re
 //   P^T  = exp2(S^T scale log2e - LSE_i log2e)           (masked, dropout bits)
 //   dS^T = P^T (dP^T Z/(1-p) - D_i)
 //   dQ_i += dS K_j            (smem x smem, added into the fp32 workspace)
-//   dV_j += (P Z/(1-p))^T dO_i,   dK_j += dS^T Q_i       (P, dS read from TMEM)
+//   dV_j += (P Z/(1-p))^T dO_i                           (P read from TMEM)
+//   dK_j += dS^T Q_i                                     (dS read from smem)
 // dK_j (times scale) and dV_j leave the chip once, at the end.
 //
 // Warp roles (448 threads):
 //   warps 0-3  compute, query columns 0-63 of the block: one thread per key
 //              row (TMEM lane) builds P and dS
 //   warps 4-7  compute, query columns 64-127
-//   warps 8-11 dQ: one thread per query row, reads dQ from TMEM and adds it
-//              into the workspace with vector atomics
+//   warps 8-11 dQ: read dQ out of TMEM and add it into the fp32 workspace
+//              with fire-and-forget reductions (d = 64: one thread per query
+//              row, 16-byte adds; d = 128: one thread per head-dim column,
+//              one 128-byte contiguous add per warp instruction)
 //   warp  12   TMA producer: K_j, V_j once; Q_i, dO_i, LSE_i, D_i per block
 //   warp  13   MMA issuer; dV/dK for query columns 0-63 start as soon as the
 //              first compute warpgroup is done
 //
 // Tensor memory (512 columns):
 //   d = 64:  dK [0,64) dV [64,128) S [128,256) dP [256,384) dQ [384,448)
-//   d = 128: dK [0,128) dV [128,256) S [256,384) dP [384,512).  Each compute
-//            warpgroup writes its P and dS (bf16 pairs) into the first 32
-//            columns of its 64-column half of S and dP; dQ's four 32-column
-//            pieces go in the remaining 32-column gaps, so the next S^T waits
-//            until the dQ warps have read dQ out.
+//   d = 128: dK [0,128) dV [128,256) S [256,384) dP [384,512); dQ^T reuses
+//            the dP columns, so the next S^T waits until the dQ warps have
+//            read it out.
+// Each compute warpgroup writes its P (bf16 pairs) over the first 32 columns
+// of its 64-column half of S.  dS goes to shared memory only: it is the
+// MN-major operand of the dQ product and, read as K-major with keys as rows,
+// the A operand of dK += dS^T Q.
 template <int D>
 struct BwdCfg {
     static constexpr int THREADS = 448;
@@ -141,16 +146,15 @@ struct BwdCfg {
     static constexpr uint32_t C_DV = D;
     static constexpr uint32_t C_S = 2 * D;
     static constexpr uint32_t C_DP = 2 * D + 128;
-    static constexpr uint32_t C_DQ = 2 * D + 256;   // d = 64 only
-    static constexpr int DQ_N = (D == 64) ? 64 : 32;  // N of one dQ MMA
+    // dQ, fp32: its own columns for d = 64; for d = 128 it reuses the dP
+    // columns, which are free once P and dS have been built.
+    static constexpr uint32_t C_DQ = (D == 64) ? 2 * D + 256 : C_DP;
     static constexpr uint32_t IDESC_SDP = idesc_f32acc(128, 128, false, false, false);
     static constexpr uint32_t IDESC_DKV = idesc_f32acc(128, D, false, false, true);
-    static constexpr uint32_t IDESC_DQ = idesc_f32acc(128, DQ_N, false, true, true);
+    // d = 64: dQ = dS K (lanes = queries, N = 64).  d = 128: dQ^T = K^T dS^T
+    // (lanes = head-dim columns, N = 128 queries).
+    static constexpr uint32_t IDESC_DQ = idesc_f32acc(128, (D == 64) ? 64 : 128, false, true, true);
     static_assert(SMEM <= 232448, "shared memory budget");
-    // TMEM column of dQ columns [32 q, 32 q + 32) when d = 128
-    __device__ static constexpr uint32_t dq_col128(int q) {
-        return (q < 2 ? C_S : C_DP) + ((q & 1) ? 96u : 32u);
-    }
 };
 
 template <int D, bool kCausal, bool kDropout>
@@ -279,28 +283,38 @@ __global__ void __launch_bounds__(448, 1)
     } else if (warp == 13) {
         // ================= MMA issuer =================
         if (lane == 0) {
-            const uint32_t sK = smem_u32(smem + C::OFF_K);
-            const uint32_t sV = smem_u32(smem + C::OFF_V);
-            const uint32_t sdS = smem_u32(smem + C::OFF_DS);
-            // dV += P^T dO and dK += dS^T Q over query columns [64 hh, 64 hh + 64)
-            auto issue_dkv_half = [&](int hh, uint32_t sQ, uint32_t sdO, bool first) {
+            // Descriptor bases built once; each MMA only adds a constant.
+            const uint64_t dK_k = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);    // K-major
+            const uint64_t dV_k = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);
+            const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + C::OFF_K), C::CB_BYTES, 1024);
+            const uint64_t dS_mn = sdesc_sw128(smem_u32(smem + C::OFF_DS), C::CB_BYTES, 1024);
+            const uint64_t dS_k = sdesc_sw128(smem_u32(smem + C::OFF_DS), 16, 1024);  // keys as rows
+            const uint64_t dQ_k0 = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+            const uint64_t dQ_mn0 = sdesc_sw128(smem_u32(smem + C::OFF_Q), C::CB_BYTES, 1024);
+            const uint64_t dO_k0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
+            const uint64_t dO_mn0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), C::CB_BYTES, 1024);
+            // dV += P^T dO (P from TMEM) and dK += dS^T Q (dS from smem) over the
+            // query columns [64 hh, 64 hh + 64)
+            auto issue_dkv_half = [&](int hh, uint64_t q_mn, uint64_t do_mn, bool first) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_ts<false>(tmem + C::C_DV, tmem + C::C_S + 64 * hh + 8 * kk,
-                                  sdesc_sw128(sdO + (4 * hh + kk) * 2048, C::CB_BYTES, 1024),
-                                  C::IDESC_DKV, (first && kk == 0) ? 0u : 1u);
+                                  sdesc_adv(do_mn, (4 * hh + kk) * 2048), C::IDESC_DKV,
+                                  (first && kk == 0) ? 0u : 1u);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ts<false>(tmem + C::C_DK, tmem + C::C_DP + 64 * hh + 8 * kk,
-                                  sdesc_sw128(sQ + (4 * hh + kk) * 2048, C::CB_BYTES, 1024),
-                                  C::IDESC_DKV, (first && kk == 0) ? 0u : 1u);
+                    mma_ss<false>(tmem + C::C_DK, sdesc_adv(dS_k, hh * C::CB_BYTES + 32 * kk),
+                                  sdesc_adv(q_mn, (4 * hh + kk) * 2048), C::IDESC_DKV,
+                                  (first && kk == 0) ? 0u : 1u);
             };
             bool ok = mbar_wait(bar_kv, 0, s_abort);
             for (int it = 0; it < nq && ok; ++it) {
                 const int stage = it & 1;
                 const uint32_t ph = (it >> 1) & 1;
-                const uint32_t sQ = smem_u32(smem + C::OFF_Q + stage * C::TILE);
-                const uint32_t sdO = smem_u32(smem + C::OFF_DO + stage * C::TILE);
+                const uint64_t q_k = sdesc_adv(dQ_k0, stage * C::TILE);
+                const uint64_t q_mn = sdesc_adv(dQ_mn0, stage * C::TILE);
+                const uint64_t do_k = sdesc_adv(dO_k0, stage * C::TILE);
+                const uint64_t do_mn = sdesc_adv(dO_mn0, stage * C::TILE);
                 ok = mbar_wait(&full_q[stage], ph, s_abort);
                 if (ok && D == 128 && it > 0) ok = mbar_wait(bar_dQfree, (it - 1) & 1, s_abort);
                 if (!ok) break;
@@ -308,41 +322,36 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
                 for (int kk = 0; kk < C::QK_STEPS; ++kk) {   // S^T = K Q^T
                     const uint32_t off = (kk >> 2) * C::CB_BYTES + (kk & 3) * 32;
-                    mma_ss<false>(tmem + C::C_S, sdesc_sw128(sK + off, 16, 1024),
-                                  sdesc_sw128(sQ + off, 16, 1024), C::IDESC_SDP, kk > 0);
+                    mma_ss<false>(tmem + C::C_S, sdesc_adv(dK_k, off), sdesc_adv(q_k, off),
+                                  C::IDESC_SDP, kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < C::QK_STEPS; ++kk) {   // dP^T = V dO^T
                     const uint32_t off = (kk >> 2) * C::CB_BYTES + (kk & 3) * 32;
-                    mma_ss<false>(tmem + C::C_DP, sdesc_sw128(sV + off, 16, 1024),
-                                  sdesc_sw128(sdO + off, 16, 1024), C::IDESC_SDP, kk > 0);
+                    mma_ss<false>(tmem + C::C_DP, sdesc_adv(dV_k, off), sdesc_adv(do_k, off),
+                                  C::IDESC_SDP, kk > 0);
                 }
                 tc_commit(bar_S);
                 ok = mbar_wait(&bar_P[0], it & 1, s_abort);
                 if (!ok) break;
                 tc_fence_after();
-                issue_dkv_half(0, sQ, sdO, it == 0);
+                issue_dkv_half(0, q_mn, do_mn, it == 0);
                 ok = mbar_wait(&bar_P[1], it & 1, s_abort);
                 if (ok && D == 64 && it > 0) ok = mbar_wait(bar_dQfree, (it - 1) & 1, s_abort);
                 if (!ok) break;
                 tc_fence_after();
+                issue_dkv_half(1, q_mn, do_mn, false);
 #pragma unroll
-                for (int kk = 0; kk < kTileRows / 16; ++kk) {   // dQ = dS K  (K = keys)
-                    const uint64_t ad = sdesc_sw128(sdS + kk * 2048, C::CB_BYTES, 1024);
-                    if constexpr (D == 64) {
-                        mma_ss<false>(tmem + C::C_DQ, ad, sdesc_sw128(sK + kk * 2048, C::CB_BYTES, 1024),
-                                      C::IDESC_DQ, kk > 0);
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            mma_ss<false>(tmem + C::dq_col128(q), ad,
-                                          sdesc_sw128(sK + (q >> 1) * C::CB_BYTES + (q & 1) * 64 + kk * 2048,
-                                                      C::CB_BYTES, 1024),
-                                          C::IDESC_DQ, kk > 0);
-                    }
+                for (int kk = 0; kk < kTileRows / 16; ++kk) {   // K = keys
+                    if constexpr (D == 64)   // dQ = dS K
+                        mma_ss<false>(tmem + C::C_DQ, sdesc_adv(dS_mn, kk * 2048),
+                                      sdesc_adv(dK_mn, kk * 2048), C::IDESC_DQ, kk > 0);
+                    else                     // dQ^T = K^T dS^T
+                        mma_ss<false>(tmem + C::C_DQ, sdesc_adv(dK_mn, kk * 2048),
+                                      sdesc_adv(dS_mn, kk * 2048), C::IDESC_DQ, kk > 0);
                 }
+                // After this commit every reader of the dS buffer (dK, dQ) is done.
                 tc_commit(bar_dQ);
-                issue_dkv_half(1, sQ, sdO, false);
                 tc_commit(&empty_q[stage]);
             }
             if (ok) tc_commit(bar_dkdv);
@@ -438,10 +447,10 @@ __global__ void __launch_bounds__(448, 1)
                     dk[e] = pack_bf16x2(ds[0], ds[1]);
                 }
                 tmem_st8(tS + 8 * c, pk);
-                tmem_st8(tdP + 8 * c, dk);
-                // dS (bf16) into shared memory as the dQ MMA's A operand: query
-                // index innermost (MN-major, one 64-query block per half), 128-byte
-                // swizzle.
+                // dS (bf16) into shared memory: query index innermost (one
+                // 64-query block per half), 128-byte swizzle.  bar_S of this block
+                // also means every MMA of the previous block (the buffer's
+                // readers) has completed.
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int chunk = (2 * c + u) ^ (r & 7);
@@ -489,44 +498,56 @@ __global__ void __launch_bounds__(448, 1)
             }
         }
     } else {
-        // ================= dQ: one query row per thread =================
-        const int rq = (warp & 3) * 32 + lane;
+        // ================= dQ: read dQ out of TMEM, add into the workspace =================
         const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         for (int it = 0; it < nq; ++it) {
-            const int i = (q_begin + it) * kTileRows + rq;
             if (!mbar_wait_warp(bar_dQ, it & 1, s_abort)) break;
             tc_fence_after();
-            float4* dst = reinterpret_cast<float4*>(p.dq_acc + (static_cast<size_t>(bh) * p.Npad + i) * D);
-            // d = 64: one 64-column piece.  d = 128: pieces 0,1 then 2,3; the
-            // TMEM columns are released after the last load.
-#pragma unroll
-            for (int half = 0; half < D / 64; ++half) {
+            const size_t row0 = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(q_begin + it) * kTileRows;
+            if constexpr (D == 64) {
+                // lane = query row rq; 64 head-dim columns as 16-byte adds
+                const int rq = (warp & 3) * 32 + lane;
                 uint32_t x[2][32];
-                if constexpr (D == 64) {
-                    tmem_ld32(tl + C::C_DQ, x[0]);
-                    tmem_ld32(tl + C::C_DQ + 32, x[1]);
-                } else {
-                    tmem_ld32(tl + C::dq_col128(2 * half), x[0]);
-                    tmem_ld32(tl + C::dq_col128(2 * half + 1), x[1]);
-                }
+                tmem_ld32(tl + C::C_DQ, x[0]);
+                tmem_ld32(tl + C::C_DQ + 32, x[1]);
                 tmem_ld_wait();
                 reg_fence(x[0]);
                 reg_fence(x[1]);
-                if (half == D / 64 - 1) {
-                    tc_fence_before();
-                    mbar_arrive(bar_dQfree);
-                }
-                if (i < N) {
+                tc_fence_before();
+                mbar_arrive(bar_dQfree);
+                if ((q_begin + it) * kTileRows + rq < N) {
+                    float* dst = p.dq_acc + (row0 + rq) * D;
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
-                            atomicAdd(dst + half * 16 + c * 8 + v,
-                                      make_float4(__uint_as_float(x[c][4 * v]),
-                                                  __uint_as_float(x[c][4 * v + 1]),
-                                                  __uint_as_float(x[c][4 * v + 2]),
-                                                  __uint_as_float(x[c][4 * v + 3])));
+                            red_add_v4(dst + 32 * c + 4 * v, __uint_as_float(x[c][4 * v]),
+                                       __uint_as_float(x[c][4 * v + 1]),
+                                       __uint_as_float(x[c][4 * v + 2]),
+                                       __uint_as_float(x[c][4 * v + 3]));
                 }
+            } else {
+                // lane = head-dim column dc; TMEM columns are the 128 queries.  All
+                // of them go to registers first, so TMEM is released before the
+                // (slow to issue) reductions start; each warp instruction then adds
+                // one query row's 32 consecutive floats.
+                const int dc = (warp & 3) * 32 + lane;
+                const int nvalid = min(kTileRows, N - (q_begin + it) * kTileRows);
+                float* col = p.dq_acc + row0 * D + dc;
+                uint32_t x[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(tl + C::C_DQ + 32 * c, x[c]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) reg_fence(x[c]);
+                tc_fence_before();
+                mbar_arrive(bar_dQfree);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (32 * c + e < nvalid)
+                            red_add_f32(col + static_cast<size_t>(32 * c + e) * D, __uint_as_float(x[c][e]));
             }
         }
     }

@@ -227,30 +227,32 @@ __global__ void __launch_bounds__(320, 1)
     } else if (warp == 9) {
         // ================= MMA issuer =================
         if (lane == 0 && nkv > 0) {
-            const uint32_t sq[2] = {smem_u32(sQ), smem_u32(sQ + C::TILE)};
-            const uint32_t skv = smem_u32(sKV);
+            // Descriptor bases built once; each MMA only adds a constant.
+            const uint64_t dq0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dq1 = sdesc_adv(dq0, C::TILE);
+            const uint64_t dk0 = sdesc_sw128(smem_u32(sKV), 16, 1024);   // K-major, slot 0
+            const uint64_t dv0 = kTF32 ? dk0 : sdesc_sw128(smem_u32(sKV), C::CB_BYTES, 1024);
             auto issue_qk = [&](int t, int slot) {
                 const uint32_t d_tmem = tmem + 128u * t;
+                const uint64_t ad = t ? dq1 : dq0;
+                const uint64_t bd = sdesc_adv(dk0, slot * C::TILE);
 #pragma unroll
                 for (int kk = 0; kk < C::QK_STEPS; ++kk) {
                     const uint32_t off = (kk >> 2) * C::CB_BYTES + (kk & 3) * 32;
-                    const uint64_t ad = sdesc_sw128(sq[t] + off, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(skv + slot * C::TILE + off, 16, 1024);
-                    mma_ss<kTF32>(d_tmem, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                    mma_ss<kTF32>(d_tmem, sdesc_adv(ad, off), sdesc_adv(bd, off), C::IDESC_QK,
+                                  kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, int slot, bool accumulate) {
                 const uint32_t d_tmem = tmem + 256u + D * t;
                 const uint32_t a_tmem = tmem + 128u * t;
+                const uint64_t bd = sdesc_adv(dv0, slot * C::TILE);
 #pragma unroll
                 for (int kk = 0; kk < C::PV_STEPS; ++kk) {
                     // bf16: V as stored (MN-major); fp32: V transposed (K-major)
-                    const uint64_t bd =
-                        kTF32 ? sdesc_sw128(skv + slot * C::TILE + (kk >> 2) * (D * 128) + (kk & 3) * 32,
-                                            16, 1024)
-                              : sdesc_sw128(skv + slot * C::TILE + kk * C::KSTEP * 128, C::CB_BYTES,
-                                            1024);
-                    mma_ts<kTF32>(d_tmem, a_tmem + kk * 8, bd, C::IDESC_PV,
+                    const uint32_t off = kTF32 ? (kk >> 2) * (D * 128) + (kk & 3) * 32
+                                               : kk * C::KSTEP * 128;
+                    mma_ts<kTF32>(d_tmem, a_tmem + kk * 8, sdesc_adv(bd, off), C::IDESC_PV,
                                   (accumulate || kk > 0) ? 1u : 0u);
                 }
             };

@@ -123,6 +123,18 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// Fire-and-forget adds into global memory (no value comes back, so the issuing
+// warp never waits on them).  red_add_v4 needs a 16-byte aligned address.
+__device__ __forceinline__ void red_add_v4(float* gptr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gptr), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void red_add_f32(float* gptr, float a) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gptr), "f"(a) : "memory");
+}
+
 // Make generic-proxy writes to shared memory visible to the async proxy (MMA
 // operand reads, TMA stores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -173,14 +185,12 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-            : "memory");
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
     } else {
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-            : "memory");
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
     }
 }
 
@@ -192,14 +202,12 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-            : "memory");
+            "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
     } else {
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-            : "memory");
+            "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
     }
 }
 
@@ -300,6 +308,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     d |= static_cast<uint64_t>(1) << 46;
     d |= static_cast<uint64_t>(2) << 61;
     return d;
+}
+
+// The same descriptor moved `bytes` (a multiple of 16) further into shared
+// memory: only the start-address field changes, and it cannot carry out of its
+// 14 bits for addresses inside the 228 KB window.
+__device__ __forceinline__ uint64_t sdesc_adv(uint64_t desc, uint32_t bytes) {
+    return desc + static_cast<uint64_t>(bytes >> 4);
 }
 
 // Instruction descriptor for kind::f16 (bf16 operands) and kind::tf32, fp32
