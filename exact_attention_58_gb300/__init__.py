@@ -27,7 +27,7 @@ from . import _build
 
 __all__ = [
     "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
-    "attn_bwd_main", "attn_bwd_dq_convert", "attn_status_string", "attn_version", "library",
+    "attn_bwd_main", "attn_bwd_dq_convert", "attn_bwd_noalloc", "attn_status_string", "attn_version", "library",
     "LIB_PATH", "STATUS",
 ]
 
@@ -73,6 +73,8 @@ def library():
                                      vp, vp]
             lib.attn_bwd.argtypes = [vp] * 9 + [ip, ip, ip, ip, ip, f, ip, vp, f, u64, vp, sz,
                                                 vp, vp]
+            lib.attn_bwd_noalloc.argtypes = [vp] * 9 + [ip, ip, ip, ip, ip, f, ip, vp, f, u64,
+                                                        vp, vp]
             lib.attn_bwd_workspace_size.argtypes = [ip, ip, ip, ip]
             lib.attn_bwd_workspace_size.restype = sz
             lib.attn_bwd_preprocess.argtypes = [vp, vp, vp, ip, ip, ip, ip, ip, vp, sz, vp]
@@ -80,7 +82,7 @@ def library():
                                                      sz, vp, vp]
             lib.attn_bwd_dq_convert.argtypes = [vp, ip, ip, ip, ip, ip, f, vp, sz, vp]
             for fn in ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
-                       "attn_bwd_dq_convert"):
+                       "attn_bwd_dq_convert", "attn_bwd_noalloc"):
                 getattr(lib, fn).restype = ctypes.c_int
             lib.attn_status_string.argtypes = [ctypes.c_int]
             lib.attn_status_string.restype = ctypes.c_char_p
@@ -206,6 +208,32 @@ def attn_bwd(q, k, v, o, do, lse, *, causal: bool = False, key_lens=None,
                             int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(ws), ws_bytes, _ptr(dev_status),
                             _stream(stream))
     _raise(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_noalloc(q, k, v, o, do, lse, *, causal: bool = False, key_lens=None,
+                     dropout_p: float = 0.0, seed: int = 0, scale: Optional[float] = None,
+                     dq=None, dk=None, dv=None, dev_status=None, stream=None):
+    """attn_bwd using the library's built-in 32 MiB scratch instead of a
+    workspace, for callers that cannot allocate device memory.  Outputs must be
+    passed in (dq, dk, dv) by such callers; see include/gbattn.h."""
+    B, H, N, d = _shape(q)
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+        _check_like(name, t, q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_like(name, t, q)
+    kl = _key_lens(key_lens, q)
+    st = library().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                    _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, _dtype_code(q),
+                                    float(scale), int(bool(causal)), _ptr(kl), float(dropout_p),
+                                    int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(dev_status),
+                                    _stream(stream))
+    _raise(st, "attn_bwd_noalloc")
     return dq, dk, dv
 
 

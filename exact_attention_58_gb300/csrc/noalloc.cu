@@ -1,0 +1,71 @@
+// noalloc.cu — attn_bwd_noalloc: the backward pass with its scratch held in a
+// buffer that lives inside this library instead of a caller-supplied workspace.
+//
+// Who needs it: callers that cannot allocate device memory where they run the
+// backward — for example a plugin inside a host framework that owns every
+// device allocation and hands its plugins no allocator, or latency-critical
+// code that must not call cudaMalloc (or any routine that allocates) on its hot
+// path.  They pass inputs and outputs only; the library supplies the scratch.
+//
+// The scratch is one file-scope __device__ array of kNoAllocScratchBytes
+// (32 MiB).  Every GPU that loads this library holds that memory until the
+// process exits.  In host code the array's name is only a host-side stand-in,
+// so its device address is looked up with cudaGetSymbolAddress, once per
+// device, on the first call made on that device (with that device current);
+// make that first call before any stream capture.  All calls share the one
+// array: the backward clears what must start at zero (the dQ accumulator) on
+// every call, but two calls that overlap on the GPU race on the array.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace gbattn {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up once).
+attn_status scratch_on_current_device(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+            return ATTN_ERR_CUDA;
+        g_scratch_addr[dev] = ptr;
+    }
+    *out = g_scratch_addr[dev];
+    return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace gbattn
+
+extern "C" attn_status attn_bwd_noalloc(const void* Q, const void* K, const void* V,
+                                        const void* O, const void* dO, const float* LSE,
+                                        void* dQ, void* dK, void* dV, int B, int H, int N, int d,
+                                        attn_dtype dtype, float scale, int causal,
+                                        const int32_t* key_lens, float dropout_p, uint64_t seed,
+                                        int* dev_status, void* stream) {
+    const size_t need = attn_bwd_workspace_size(B, H, N, d);
+    const bool null_arg = !Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV;
+    if (need == 0 || null_arg)   // rejected arguments: attn_bwd says why, before any CUDA call
+        return attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, dtype, scale, causal,
+                        key_lens, dropout_p, seed, nullptr, 0, dev_status, stream);
+    if (need > gbattn::kNoAllocScratchBytes) return ATTN_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    const attn_status st = gbattn::scratch_on_current_device(&scratch);
+    if (st != ATTN_OK) return st;
+    return attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, dtype, scale, causal, key_lens,
+                    dropout_p, seed, scratch, gbattn::kNoAllocScratchBytes, dev_status, stream);
+}

@@ -140,6 +140,31 @@ attn_status attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, attn_dtype
                                 float scale, const void* workspace, size_t workspace_bytes,
                                 void* stream);
 
+/*
+ * attn_bwd without a workspace argument, for callers that cannot allocate
+ * device memory where they run the backward (a plugin inside a framework that
+ * owns every device allocation and gives it no allocator, or latency-critical
+ * code that must not call cudaMalloc).  The pages have no counterpart: this is
+ * a deployment convenience, not part of the method.
+ *   Scratch   a 32 MiB buffer inside the library (a file-scope __device__
+ *             array), held by every GPU that loads the library until exit.
+ *             Shapes whose attn_bwd_workspace_size exceeds 32 MiB are
+ *             rejected with ATTN_ERR_WORKSPACE before anything is enqueued.
+ *   Set-up    the first call on a device looks up the buffer's device address
+ *             (cudaGetSymbolAddress) with that device current; make that first
+ *             call before any stream capture.
+ *   Sharing   every call uses the same buffer; each call clears what must
+ *             start at zero, but calls that overlap on the GPU race on it.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * Otherwise identical to attn_bwd (same arguments minus the workspace, same
+ * results, same errors).
+ */
+attn_status attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                             const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                             int B, int H, int N, int d, attn_dtype dtype, float scale,
+                             int causal, const int32_t* key_lens, float dropout_p,
+                             uint64_t seed, int* dev_status, void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* attn_status_string(attn_status status);
 
