@@ -112,13 +112,17 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(__nv_bfloat16* __re
 //              row, 16-byte adds; d = 128: one thread per head-dim column,
 //              one 128-byte contiguous add per warp instruction)
 //   warp  12   TMA producer: K_j, V_j once; Q_i, dO_i, LSE_i, D_i per block
-//   warp  13   MMA issuer; dV/dK for query columns 0-63 start as soon as the
-//              first compute warpgroup is done
+//   warp  13   MMA issuer.  S^T and dP^T are committed separately: the
+//              compute warps build P from S^T while dP^T runs, dV for each
+//              query half starts as soon as its P is in TMEM, and dK for each
+//              half as soon as its dS is in shared memory.  Across blocks the
+//              issue order is  dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1}, so the
+//              next S^T is computed while the compute warps build dS_i.
 //
 // Tensor memory (512 columns):
 //   d = 64:  dK [0,64) dV [64,128) S [128,256) dP [256,384) dQ [384,448)
 //   d = 128: dK [0,128) dV [128,256) S [256,384) dP [384,512); dQ^T reuses
-//            the dP columns, so the next S^T waits until the dQ warps have
+//            the dP columns, so the next dP^T waits until the dQ warps have
 //            read it out.
 // Each compute warpgroup writes its P (bf16 pairs) over the first 32 columns
 // of its 64-column half of S.  dS goes to shared memory only: it is the
@@ -131,6 +135,7 @@ struct BwdCfg {
     static constexpr int NCB = ROWB / 128;
     static constexpr int TILE = kTileRows * ROWB;
     static constexpr int CB_BYTES = kTileRows * 128;
+    static constexpr int HALF_BYTES = CB_BYTES / 2;   // 64 rows of one 128-byte column block
     static constexpr int DS_BYTES = kTileRows * kTileRows * 2;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = TILE;
@@ -140,7 +145,7 @@ struct BwdCfg {
     static constexpr int OFF_LSE = OFF_DS + DS_BYTES;   // [2][128] float
     static constexpr int OFF_D = OFF_LSE + 1024;        // [2][128] float
     static constexpr int OFF_BAR = OFF_D + 1024;
-    static constexpr int SMEM = OFF_BAR + 128;
+    static constexpr int SMEM = OFF_BAR + 256;
     static constexpr int QK_STEPS = ROWB / 32;
     static constexpr uint32_t C_DK = 0;
     static constexpr uint32_t C_DV = D;
@@ -150,10 +155,11 @@ struct BwdCfg {
     // columns, which are free once P and dS have been built.
     static constexpr uint32_t C_DQ = (D == 64) ? 2 * D + 256 : C_DP;
     static constexpr uint32_t IDESC_SDP = idesc_f32acc(128, 128, false, false, false);
+    static constexpr uint32_t IDESC_DP_HALF = idesc_f32acc(128, 64, false, false, false);
     static constexpr uint32_t IDESC_DKV = idesc_f32acc(128, D, false, false, true);
     // d = 64: dQ = dS K (lanes = queries, N = 64).  d = 128: dQ^T = K^T dS^T
-    // (lanes = head-dim columns, N = 128 queries).
-    static constexpr uint32_t IDESC_DQ = idesc_f32acc(128, (D == 64) ? 64 : 128, false, true, true);
+    // (lanes = head-dim columns), one N = 64 product per query half.
+    static constexpr uint32_t IDESC_DQ = idesc_f32acc(128, 64, false, true, true);
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -207,13 +213,15 @@ __global__ void __launch_bounds__(448, 1)
     uint64_t* bar_kv = bars + 0;
     uint64_t* full_q = bars + 1;      // [2]
     uint64_t* empty_q = bars + 3;     // [2]
-    uint64_t* bar_S = bars + 5;
-    uint64_t* bar_P = bars + 6;       // [2] one per compute warpgroup
-    uint64_t* bar_dQ = bars + 8;
-    uint64_t* bar_dQfree = bars + 9;
-    uint64_t* bar_dkdv = bars + 10;
-    uint64_t* bar_fin = bars + 11;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 12);
+    uint64_t* bar_S = bars + 5;       // S^T in TMEM
+    uint64_t* bar_P = bars + 6;       // [2] P of a query half in TMEM (one per warpgroup)
+    uint64_t* bar_dQ = bars + 8;       // [2] dQ (d = 128: each query half of dQ^T) in TMEM
+    uint64_t* bar_dQfree = bars + 10;  // [2] the dQ warps have read it out
+    uint64_t* bar_dkdv = bars + 12;
+    uint64_t* bar_fin = bars + 13;
+    uint64_t* bar_dP = bars + 14;      // [2] dP^T of a query half in TMEM
+    uint64_t* bar_dS = bars + 16;      // [2] dS of a query half in smem
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 18);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
     float* sLSE = reinterpret_cast<float*>(smem + C::OFF_LSE);
     float* sD = reinterpret_cast<float*>(smem + C::OFF_D);
@@ -224,10 +232,12 @@ __global__ void __launch_bounds__(448, 1)
             mbar_init(&full_q[s], 1);
             mbar_init(&empty_q[s], 1);
             mbar_init(&bar_P[s], kTileRows);
+            mbar_init(&bar_dS[s], kTileRows);
+            mbar_init(&bar_dP[s], 1);
+            mbar_init(&bar_dQ[s], 1);
+            mbar_init(&bar_dQfree[s], kTileRows);
         }
         mbar_init(bar_S, 1);
-        mbar_init(bar_dQ, 1);
-        mbar_init(bar_dQfree, kTileRows);
         mbar_init(bar_dkdv, 1);
         mbar_init(bar_fin, 1);
         *s_abort = 0;
@@ -295,64 +305,121 @@ __global__ void __launch_bounds__(448, 1)
             const uint64_t dO_mn0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), C::CB_BYTES, 1024);
             // dV += P^T dO (P from TMEM) and dK += dS^T Q (dS from smem) over the
             // query columns [64 hh, 64 hh + 64)
-            auto issue_dkv_half = [&](int hh, uint64_t q_mn, uint64_t do_mn, bool first) {
+            auto issue_dv_half = [&](int hh, uint64_t do_mn, bool first) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_ts<false>(tmem + C::C_DV, tmem + C::C_S + 64 * hh + 8 * kk,
                                   sdesc_adv(do_mn, (4 * hh + kk) * 2048), C::IDESC_DKV,
                                   (first && kk == 0) ? 0u : 1u);
+            };
+            auto issue_dk_half = [&](int hh, uint64_t q_mn, bool first) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_ss<false>(tmem + C::C_DK, sdesc_adv(dS_k, hh * C::CB_BYTES + 32 * kk),
                                   sdesc_adv(q_mn, (4 * hh + kk) * 2048), C::IDESC_DKV,
                                   (first && kk == 0) ? 0u : 1u);
             };
-            bool ok = mbar_wait(bar_kv, 0, s_abort);
-            for (int it = 0; it < nq && ok; ++it) {
-                const int stage = it & 1;
-                const uint32_t ph = (it >> 1) & 1;
+            auto issue_s = [&](int stage) {   // S^T = K Q^T
                 const uint64_t q_k = sdesc_adv(dQ_k0, stage * C::TILE);
-                const uint64_t q_mn = sdesc_adv(dQ_mn0, stage * C::TILE);
-                const uint64_t do_k = sdesc_adv(dO_k0, stage * C::TILE);
-                const uint64_t do_mn = sdesc_adv(dO_mn0, stage * C::TILE);
-                ok = mbar_wait(&full_q[stage], ph, s_abort);
-                if (ok && D == 128 && it > 0) ok = mbar_wait(bar_dQfree, (it - 1) & 1, s_abort);
-                if (!ok) break;
-                tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < C::QK_STEPS; ++kk) {   // S^T = K Q^T
+                for (int kk = 0; kk < C::QK_STEPS; ++kk) {
                     const uint32_t off = (kk >> 2) * C::CB_BYTES + (kk & 3) * 32;
                     mma_ss<false>(tmem + C::C_S, sdesc_adv(dK_k, off), sdesc_adv(q_k, off),
                                   C::IDESC_SDP, kk > 0);
                 }
+            };
+            // dP^T = V dO^T for the query columns [64 hh, 64 hh + 64) (N = 64:
+            // B is rows 64 hh.. of the dO tile)
+            auto issue_dp_half = [&](int stage, int hh) {
+                const uint64_t do_k = sdesc_adv(dO_k0, stage * C::TILE + hh * C::HALF_BYTES);
 #pragma unroll
-                for (int kk = 0; kk < C::QK_STEPS; ++kk) {   // dP^T = V dO^T
+                for (int kk = 0; kk < C::QK_STEPS; ++kk) {
                     const uint32_t off = (kk >> 2) * C::CB_BYTES + (kk & 3) * 32;
-                    mma_ss<false>(tmem + C::C_DP, sdesc_adv(dV_k, off), sdesc_adv(do_k, off),
-                                  C::IDESC_SDP, kk > 0);
+                    mma_ss<false>(tmem + C::C_DP + 64 * hh, sdesc_adv(dV_k, off),
+                                  sdesc_adv(do_k, off), C::IDESC_DP_HALF, kk > 0);
                 }
-                tc_commit(bar_S);
-                ok = mbar_wait(&bar_P[0], it & 1, s_abort);
-                if (!ok) break;
-                tc_fence_after();
-                issue_dkv_half(0, q_mn, do_mn, it == 0);
-                ok = mbar_wait(&bar_P[1], it & 1, s_abort);
-                if (ok && D == 64 && it > 0) ok = mbar_wait(bar_dQfree, (it - 1) & 1, s_abort);
-                if (!ok) break;
-                tc_fence_after();
-                issue_dkv_half(1, q_mn, do_mn, false);
+            };
+            // d = 128: the next dP^T half may only land once the dQ warps have
+            // read the dQ^T half that shares its columns.
+            auto issue_dp = [&](int stage, int it_prev) {
 #pragma unroll
-                for (int kk = 0; kk < kTileRows / 16; ++kk) {   // K = keys
-                    if constexpr (D == 64)   // dQ = dS K
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (D == 128 && it_prev >= 0 &&
+                        !mbar_wait(&bar_dQfree[hh], it_prev & 1, s_abort))
+                        return false;
+                    tc_fence_after();
+                    issue_dp_half(stage, hh);
+                    tc_commit(&bar_dP[hh]);
+                }
+                return true;
+            };
+            // Software pipeline over query blocks: S^T of block i+1 is issued
+            // right behind dV of block i (the tensor pipe runs one thread's MMAs
+            // in issue order, so it reads P_i before S^T_{i+1} overwrites it),
+            // and dP^T of block i+1 right behind dQ and dK of block i.  The
+            // compute warps then always find the next S^T on its way while
+            // they build dS.
+            bool ok = mbar_wait(bar_kv, 0, s_abort) && mbar_wait(&full_q[0], 0, s_abort);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                tc_commit(bar_S);
+                ok = issue_dp(0, -1);
+            }
+            for (int it = 0; it < nq && ok; ++it) {
+                const int stage = it & 1;
+                const bool more = it + 1 < nq;
+                const int nstage = stage ^ 1;
+                const uint64_t q_mn = sdesc_adv(dQ_mn0, stage * C::TILE);
+                const uint64_t do_mn = sdesc_adv(dO_mn0, stage * C::TILE);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {   // dV += P^T dO as soon as each half of P is in
+                    ok = mbar_wait(&bar_P[hh], it & 1, s_abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_dv_half(hh, do_mn, it == 0 && hh == 0);
+                }
+                if (!ok) break;
+                if (more) {
+                    ok = mbar_wait(&full_q[nstage], ((it + 1) >> 1) & 1, s_abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(nstage);
+                    tc_commit(bar_S);
+                }
+                ok = mbar_wait(&bar_dS[0], it & 1, s_abort);
+                if (!ok) break;
+                tc_fence_after();
+                issue_dk_half(0, q_mn, it == 0);
+                ok = mbar_wait(&bar_dS[1], it & 1, s_abort);
+                if (ok && D == 64 && it > 0) ok = mbar_wait(&bar_dQfree[0], (it - 1) & 1, s_abort);
+                if (!ok) break;
+                tc_fence_after();
+                if constexpr (D == 64) {   // dQ = dS K
+#pragma unroll
+                    for (int kk = 0; kk < kTileRows / 16; ++kk)   // K = keys
                         mma_ss<false>(tmem + C::C_DQ, sdesc_adv(dS_mn, kk * 2048),
                                       sdesc_adv(dK_mn, kk * 2048), C::IDESC_DQ, kk > 0);
-                    else                     // dQ^T = K^T dS^T
-                        mma_ss<false>(tmem + C::C_DQ, sdesc_adv(dK_mn, kk * 2048),
-                                      sdesc_adv(dS_mn, kk * 2048), C::IDESC_DQ, kk > 0);
+                    tc_commit(&bar_dQ[0]);
+                } else {   // dQ^T = K^T dS^T, one query half at a time, into the dP columns
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                        for (int kk = 0; kk < kTileRows / 16; ++kk)
+                            mma_ss<false>(tmem + C::C_DQ + 64 * hh, sdesc_adv(dK_mn, kk * 2048),
+                                          sdesc_adv(dS_mn, hh * C::CB_BYTES + kk * 2048),
+                                          C::IDESC_DQ, kk > 0);
+                        tc_commit(&bar_dQ[hh]);
+                    }
                 }
-                // After this commit every reader of the dS buffer (dK, dQ) is done.
-                tc_commit(bar_dQ);
+                issue_dk_half(1, q_mn, false);   // runs while the dQ warps drain dQ
                 tc_commit(&empty_q[stage]);
+                if (more) {
+                    // dP^T of the next block.  Its commits also cover dK and dQ
+                    // of this block: when they fire, the dS buffer is free.
+                    ok = issue_dp(nstage, it);
+                    if (!ok) break;
+                }
             }
             if (ok) tc_commit(bar_dkdv);
             tc_commit(bar_fin);
@@ -368,7 +435,7 @@ __global__ void __launch_bounds__(448, 1)
         const int j = k0 + r;
         const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const uint32_t tS = tl + C::C_S + 64 * hh;
-        const uint32_t tdP = tl + C::C_DP + 64 * hh;
+        const uint32_t tdP = tl + C::C_DP + 64 * hh;   // this half's dP^T columns
         const bool row_valid = j < L;
         uint8_t* rowp = smem + C::OFF_DS + hh * C::CB_BYTES + r * 128;
         bool ok = true;
@@ -386,21 +453,19 @@ __global__ void __launch_bounds__(448, 1)
             const float* d_s = sD + stage * kTileRows + 64 * hh;
             const int q0h = qi * kTileRows + 64 * hh;   // first query of this half
             const bool diag = kCausal && (qi == kb);
-            // 16-column chunks; the next chunk's TMEM loads overlap this chunk's math.
-            uint32_t sbuf[2][16], dbuf[2][16];
-            tmem_ld16(tS, sbuf[0]);
-            tmem_ld16(tdP, dbuf[0]);
+            // ---- phase 1 (while dP^T is still on the tensor pipe): P from S ----
+            // 16-column chunks; the next chunk's TMEM load overlaps this chunk's
+            // math.  P (undropped, fp32) stays in registers for phase 2.
+            float pr[64];
+            uint32_t keepw[4];
+            uint32_t buf[2][16];
+            tmem_ld16(tS, buf[0]);
             tmem_ld_wait();
-            reg_fence(sbuf[0]);
-            reg_fence(dbuf[0]);
+            reg_fence(buf[0]);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                if (c < 3) {
-                    tmem_ld16(tS + 16 * (c + 1), sbuf[(c + 1) & 1]);
-                    tmem_ld16(tdP + 16 * (c + 1), dbuf[(c + 1) & 1]);
-                }
-                const uint32_t* sv = sbuf[c & 1];
-                const uint32_t* dpv = dbuf[c & 1];
+                if (c < 3) tmem_ld16(tS + 16 * (c + 1), buf[(c + 1) & 1]);
+                const uint32_t* sv = buf[c & 1];
                 uint32_t keep = 0xFFFFu;   // bit e: column 16c+e of this half kept
                 if constexpr (kDropout) {
                     // Lanes 4m..4m+3 own keys 4m..4m+3 of one Philox counter
@@ -422,35 +487,66 @@ __global__ void __launch_bounds__(448, 1)
                             keep |= ((v >> (4 * a2 + e)) & 1u) << (4 * g + a2);
                     }
                 }
-                uint32_t pk[8], dk[8];
+                keepw[c] = keep;
+                uint32_t pk[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    float pd[2], ds[2];
+                    float pd[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int col = 16 * c + 2 * e + u;
-                        float pr = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), p.scale_log2,
-                                                   -lse_s[col]));
+                        float x = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), p.scale_log2,
+                                                  -lse_s[col]));
                         const bool valid = row_valid && (!diag || j <= q0h + col);
-                        pr = valid ? pr : 0.f;
-                        float dp = __uint_as_float(dpv[2 * e + u]);
-                        float pdrop = pr;
-                        if constexpr (kDropout) {
-                            const bool z = (keep >> (2 * e + u)) & 1u;
-                            pdrop = z ? pr * p.drop_scale : 0.f;
-                            dp = z ? dp * p.drop_scale : 0.f;
-                        }
-                        pd[u] = pdrop;
-                        ds[u] = pr * (dp - d_s[col]);
+                        x = valid ? x : 0.f;
+                        pr[col] = x;
+                        pd[u] = x;
+                        if constexpr (kDropout)
+                            pd[u] = ((keep >> (2 * e + u)) & 1u) ? x * p.drop_scale : 0.f;
                     }
                     pk[e] = pack_bf16x2(pd[0], pd[1]);
-                    dk[e] = pack_bf16x2(ds[0], ds[1]);
                 }
                 tmem_st8(tS + 8 * c, pk);
+                if (c < 3) {
+                    tmem_ld_wait();
+                    reg_fence(buf[(c + 1) & 1]);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bar_P[hh]);
+
+            // ---- phase 2: dS = P (dP Z/(1-p) - D) once dP^T is in ----
+            if (!mbar_wait_warp(&bar_dP[hh], it & 1, s_abort)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            tmem_ld16(tdP, buf[0]);
+            tmem_ld_wait();
+            reg_fence(buf[0]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (c < 3) tmem_ld16(tdP + 16 * (c + 1), buf[(c + 1) & 1]);
+                const uint32_t* dpv = buf[c & 1];
+                uint32_t dk[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    float ds[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int col = 16 * c + 2 * e + u;
+                        float dp = __uint_as_float(dpv[2 * e + u]);
+                        if constexpr (kDropout)
+                            dp = ((keepw[c] >> (2 * e + u)) & 1u) ? dp * p.drop_scale : 0.f;
+                        ds[u] = pr[col] * (dp - d_s[col]);
+                    }
+                    dk[e] = pack_bf16x2(ds[0], ds[1]);
+                }
                 // dS (bf16) into shared memory: query index innermost (one
-                // 64-query block per half), 128-byte swizzle.  bar_S of this block
-                // also means every MMA of the previous block (the buffer's
-                // readers) has completed.
+                // 64-query block per half), 128-byte swizzle.  bar_dP of this
+                // block also means every MMA of the previous block (among them
+                // the buffer's readers, dK and dQ) has completed.
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int chunk = (2 * c + u) ^ (r & 7);
@@ -459,14 +555,12 @@ __global__ void __launch_bounds__(448, 1)
                 }
                 if (c < 3) {
                     tmem_ld_wait();
-                    reg_fence(sbuf[(c + 1) & 1]);
-                    reg_fence(dbuf[(c + 1) & 1]);
+                    reg_fence(buf[(c + 1) & 1]);
                 }
             }
-            tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bar_P[hh]);
+            mbar_arrive(&bar_dS[hh]);
         }
         // ---- epilogue: warpgroup 0 writes dK = scale * acc, warpgroup 1 dV ----
         if (ok) {
@@ -501,11 +595,11 @@ __global__ void __launch_bounds__(448, 1)
         // ================= dQ: read dQ out of TMEM, add into the workspace =================
         const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         for (int it = 0; it < nq; ++it) {
-            if (!mbar_wait_warp(bar_dQ, it & 1, s_abort)) break;
-            tc_fence_after();
             const size_t row0 = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(q_begin + it) * kTileRows;
             if constexpr (D == 64) {
                 // lane = query row rq; 64 head-dim columns as 16-byte adds
+                if (!mbar_wait_warp(&bar_dQ[0], it & 1, s_abort)) break;
+                tc_fence_after();
                 const int rq = (warp & 3) * 32 + lane;
                 uint32_t x[2][32];
                 tmem_ld32(tl + C::C_DQ, x[0]);
@@ -514,7 +608,7 @@ __global__ void __launch_bounds__(448, 1)
                 reg_fence(x[0]);
                 reg_fence(x[1]);
                 tc_fence_before();
-                mbar_arrive(bar_dQfree);
+                mbar_arrive(&bar_dQfree[0]);
                 if ((q_begin + it) * kTileRows + rq < N) {
                     float* dst = p.dq_acc + (row0 + rq) * D;
 #pragma unroll
@@ -527,27 +621,42 @@ __global__ void __launch_bounds__(448, 1)
                                        __uint_as_float(x[c][4 * v + 3]));
                 }
             } else {
-                // lane = head-dim column dc; TMEM columns are the 128 queries.  All
-                // of them go to registers first, so TMEM is released before the
-                // (slow to issue) reductions start; each warp instruction then adds
-                // one query row's 32 consecutive floats.
+                // lane = head-dim column dc; TMEM columns are queries.  Each
+                // query half goes to registers whole, so its columns are released
+                // (for the next dP^T half) before the reductions start; each warp
+                // instruction then adds one query row's 32 consecutive floats.
+                // Holding one half (64 values) rather than all 128 keeps the
+                // warp inside its register budget.
                 const int dc = (warp & 3) * 32 + lane;
                 const int nvalid = min(kTileRows, N - (q_begin + it) * kTileRows);
                 float* col = p.dq_acc + row0 * D + dc;
-                uint32_t x[4][32];
+                bool ok = true;
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (!mbar_wait_warp(&bar_dQ[hh], it & 1, s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t x[2][32];
+                    tmem_ld32(tl + C::C_DQ + 64 * hh, x[0]);
+                    tmem_ld32(tl + C::C_DQ + 64 * hh + 32, x[1]);
+                    tmem_ld_wait();
+                    reg_fence(x[0]);
+                    reg_fence(x[1]);
+                    tc_fence_before();
+                    mbar_arrive(&bar_dQfree[hh]);
+                    const int nv = nvalid - 64 * hh;   // valid query rows of this half
+                    float* colh = col + static_cast<size_t>(64 * hh) * D;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tl + C::C_DQ + 32 * c, x[c]);
-                tmem_ld_wait();
+                    for (int c = 0; c < 2; ++c)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) reg_fence(x[c]);
-                tc_fence_before();
-                mbar_arrive(bar_dQfree);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (32 * c + e < nvalid)
-                            red_add_f32(col + static_cast<size_t>(32 * c + e) * D, __uint_as_float(x[c][e]));
+                        for (int e = 0; e < 32; ++e)
+                            if (32 * c + e < nv)
+                                red_add_f32(colh + static_cast<size_t>(32 * c + e) * D,
+                                            __uint_as_float(x[c][e]));
+                }
+                if (!ok) break;
             }
         }
     }
