@@ -169,9 +169,10 @@ attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const voi
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(dK) ||
         !aligned16(dV))
         return ATTN_ERR_MISALIGNED;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
     if (!make_tmap_bhnd(&tq, Q, false, B * H, N, d) || !make_tmap_bhnd(&tk, K, false, B * H, N, d) ||
-        !make_tmap_bhnd(&tv, V, false, B * H, N, d) || !make_tmap_bhnd(&tdo, dO, false, B * H, N, d))
+        !make_tmap_bhnd(&tv, V, false, B * H, N, d) || !make_tmap_bhnd(&tdo, dO, false, B * H, N, d) ||
+        !make_tmap_bhnd(&tdk, dK, false, B * H, N, d) || !make_tmap_bhnd(&tdv, dV, false, B * H, N, d))
         return ATTN_ERR_CUDA;
     const Workspace w = carve(workspace, B, H, N);
     BwdParams p{};
@@ -193,7 +194,7 @@ attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const voi
     p.drop_threshold = drop_threshold(dropout_p);
     p.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFu);
     p.seed_hi = static_cast<uint32_t>(seed >> 32);
-    return from_cuda(launch_bwd_main(tq, tk, tv, tdo, p, d, causal != 0, dropout_p > 0.f,
+    return from_cuda(launch_bwd_main(tq, tk, tv, tdo, tdk, tdv, p, d, causal != 0, dropout_p > 0.f,
                                      static_cast<cudaStream_t>(stream)));
 }
 

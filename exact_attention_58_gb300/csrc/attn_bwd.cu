@@ -168,7 +168,9 @@ __global__ void __launch_bounds__(448, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV,
-                    const __grid_constant__ CUtensorMap tmdO, const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tmdO,
+                    const __grid_constant__ CUtensorMap tmdK,
+                    const __grid_constant__ CUtensorMap tmdV, const BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
@@ -387,30 +389,33 @@ __global__ void __launch_bounds__(448, 1)
                     issue_s(nstage);
                     tc_commit(bar_S);
                 }
+                // d = 128: dQ^T = K^T dS^T for one query half needs only that
+                // half of dS, so it follows dK of the half straight away.
+                auto issue_dq_half = [&](int hh) {
+#pragma unroll
+                    for (int kk = 0; kk < kTileRows / 16; ++kk)   // K = keys
+                        mma_ss<false>(tmem + C::C_DQ + 64 * hh, sdesc_adv(dK_mn, kk * 2048),
+                                      sdesc_adv(dS_mn, hh * C::CB_BYTES + kk * 2048),
+                                      C::IDESC_DQ, kk > 0);
+                    tc_commit(&bar_dQ[hh]);
+                };
                 ok = mbar_wait(&bar_dS[0], it & 1, s_abort);
                 if (!ok) break;
                 tc_fence_after();
                 issue_dk_half(0, q_mn, it == 0);
+                if constexpr (D == 128) issue_dq_half(0);
                 ok = mbar_wait(&bar_dS[1], it & 1, s_abort);
                 if (ok && D == 64 && it > 0) ok = mbar_wait(&bar_dQfree[0], (it - 1) & 1, s_abort);
                 if (!ok) break;
                 tc_fence_after();
-                if constexpr (D == 64) {   // dQ = dS K
+                if constexpr (D == 64) {   // dQ = dS K (lanes = queries)
 #pragma unroll
                     for (int kk = 0; kk < kTileRows / 16; ++kk)   // K = keys
                         mma_ss<false>(tmem + C::C_DQ, sdesc_adv(dS_mn, kk * 2048),
                                       sdesc_adv(dK_mn, kk * 2048), C::IDESC_DQ, kk > 0);
                     tc_commit(&bar_dQ[0]);
-                } else {   // dQ^T = K^T dS^T, one query half at a time, into the dP columns
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                        for (int kk = 0; kk < kTileRows / 16; ++kk)
-                            mma_ss<false>(tmem + C::C_DQ + 64 * hh, sdesc_adv(dK_mn, kk * 2048),
-                                          sdesc_adv(dS_mn, hh * C::CB_BYTES + kk * 2048),
-                                          C::IDESC_DQ, kk > 0);
-                        tc_commit(&bar_dQ[hh]);
-                    }
+                } else {
+                    issue_dq_half(1);
                 }
                 issue_dk_half(1, q_mn, false);   // runs while the dQ warps drain dQ
                 tc_commit(&empty_q[stage]);
@@ -488,6 +493,15 @@ __global__ void __launch_bounds__(448, 1)
                     }
                 }
                 keepw[c] = keep;
+                float lv[16];   // this chunk's LSE values, four 16-byte shared loads
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const float4 t4 = reinterpret_cast<const float4*>(lse_s + 16 * c)[v];
+                    lv[4 * v] = t4.x;
+                    lv[4 * v + 1] = t4.y;
+                    lv[4 * v + 2] = t4.z;
+                    lv[4 * v + 3] = t4.w;
+                }
                 uint32_t pk[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -496,7 +510,7 @@ __global__ void __launch_bounds__(448, 1)
                     for (int u = 0; u < 2; ++u) {
                         const int col = 16 * c + 2 * e + u;
                         float x = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), p.scale_log2,
-                                                  -lse_s[col]));
+                                                  -lv[2 * e + u]));
                         const bool valid = row_valid && (!diag || j <= q0h + col);
                         x = valid ? x : 0.f;
                         pr[col] = x;
@@ -529,6 +543,15 @@ __global__ void __launch_bounds__(448, 1)
             for (int c = 0; c < 4; ++c) {
                 if (c < 3) tmem_ld16(tdP + 16 * (c + 1), buf[(c + 1) & 1]);
                 const uint32_t* dpv = buf[c & 1];
+                float dv[16];   // this chunk's D values
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const float4 t4 = reinterpret_cast<const float4*>(d_s + 16 * c)[v];
+                    dv[4 * v] = t4.x;
+                    dv[4 * v + 1] = t4.y;
+                    dv[4 * v + 2] = t4.z;
+                    dv[4 * v + 3] = t4.w;
+                }
                 uint32_t dk[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -539,7 +562,7 @@ __global__ void __launch_bounds__(448, 1)
                         float dp = __uint_as_float(dpv[2 * e + u]);
                         if constexpr (kDropout)
                             dp = ((keepw[c] >> (2 * e + u)) & 1u) ? dp * p.drop_scale : 0.f;
-                        ds[u] = pr[col] * (dp - d_s[col]);
+                        ds[u] = pr[col] * (dp - dv[2 * e + u]);
                     }
                     dk[e] = pack_bf16x2(ds[0], ds[1]);
                 }
@@ -563,33 +586,44 @@ __global__ void __launch_bounds__(448, 1)
             mbar_arrive(&bar_dS[hh]);
         }
         // ---- epilogue: warpgroup 0 writes dK = scale * acc, warpgroup 1 dV ----
+        // Each thread puts its key row (bf16) into the freed Q stage buffers in
+        // the tensor map's 128-byte swizzled layout; one thread per warpgroup
+        // then stores the whole 128-row tile with TMA (full-line writes; rows
+        // past N are clipped by the map).
         if (ok) {
             ok = mbar_wait_warp(bar_dkdv, 0, s_abort);
             tc_fence_after();
         }
+        uint8_t* stg = smem + C::OFF_Q + hh * C::TILE;   // free once bar_dkdv has fired
         if (ok) {
             const uint32_t src = tl + (hh == 0 ? C::C_DK : C::C_DV);
             const float mul = (hh == 0) ? p.scale : 1.f;
-            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(hh == 0 ? p.dK : p.dV);
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 32; ++c) {   // 32 columns = half a 128-byte column block
                 uint32_t a[32];
                 tmem_ld32(src + 32 * c, a);
                 tmem_ld_wait();
                 reg_fence(a);
-                if (j < N) {
-                    uint4* dst = reinterpret_cast<uint4*>(out + head_off + static_cast<size_t>(j) * D + 32 * c);
+                uint8_t* rowp = stg + (c >> 1) * C::CB_BYTES + r * 128;
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t w[4];
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t w[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = pack_bf16x2(__uint_as_float(a[8 * q4 + 2 * e]) * mul,
-                                               __uint_as_float(a[8 * q4 + 2 * e + 1]) * mul);
-                        dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = pack_bf16x2(__uint_as_float(a[8 * q4 + 2 * e]) * mul,
+                                           __uint_as_float(a[8 * q4 + 2 * e + 1]) * mul);
+                    const int chunk = (4 * (c & 1) + q4) ^ (r & 7);
+                    *reinterpret_cast<uint4*>(rowp + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
+            fence_proxy_async_smem();
+        }
+        named_barrier_sync(1 + hh, 128);
+        if (ok && quarter == 0 && lane == 0) {
+            const CUtensorMap* m = (hh == 0) ? &tmdK : &tmdV;
+            for (int cb = 0; cb < C::NCB; ++cb) tma_store_3d(m, stg + cb * C::CB_BYTES, cb * 64, k0, bh);
+            bulk_commit_group();
+            bulk_wait_group_read_all();
         }
     } else {
         // ================= dQ: read dQ out of TMEM, add into the workspace =================
@@ -671,7 +705,8 @@ __global__ void __launch_bounds__(448, 1)
 
 template <int D, bool kCausal, bool kDropout>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+                         const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                         const BwdParams& p, cudaStream_t stream) {
     using C = BwdCfg<D>;
     auto kern = attn_bwd_kernel<D, kCausal, kDropout>;
     static bool configured = false;
@@ -681,19 +716,19 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
         configured = true;
     }
     const unsigned grid = static_cast<unsigned>(p.nkb) * static_cast<unsigned>(p.B * p.H);
-    kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+    kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdk, tdv, p);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t dispatch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, const BwdParams& p, bool causal, bool dropout,
-                         cudaStream_t s) {
+                         const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                         const BwdParams& p, bool causal, bool dropout, cudaStream_t s) {
     if (causal)
-        return dropout ? launch_bwd_t<D, true, true>(tq, tk, tv, tdo, p, s)
-                       : launch_bwd_t<D, true, false>(tq, tk, tv, tdo, p, s);
-    return dropout ? launch_bwd_t<D, false, true>(tq, tk, tv, tdo, p, s)
-                   : launch_bwd_t<D, false, false>(tq, tk, tv, tdo, p, s);
+        return dropout ? launch_bwd_t<D, true, true>(tq, tk, tv, tdo, tdk, tdv, p, s)
+                       : launch_bwd_t<D, true, false>(tq, tk, tv, tdo, tdk, tdv, p, s);
+    return dropout ? launch_bwd_t<D, false, true>(tq, tk, tv, tdo, tdk, tdv, p, s)
+                   : launch_bwd_t<D, false, false>(tq, tk, tv, tdo, tdk, tdv, p, s);
 }
 
 }  // namespace
@@ -726,10 +761,11 @@ cudaError_t launch_bwd_dq_convert(void* dQ, const float* dq_acc, int BH, int N, 
 }
 
 cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdParams& p, int d, bool causal,
-                            bool dropout, cudaStream_t stream) {
-    if (d == 64) return dispatch_bwd<64>(tq, tk, tv, tdo, p, causal, dropout, stream);
-    if (d == 128) return dispatch_bwd<128>(tq, tk, tv, tdo, p, causal, dropout, stream);
+                            const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                            const BwdParams& p, int d, bool causal, bool dropout,
+                            cudaStream_t stream) {
+    if (d == 64) return dispatch_bwd<64>(tq, tk, tv, tdo, tdk, tdv, p, causal, dropout, stream);
+    if (d == 128) return dispatch_bwd<128>(tq, tk, tv, tdo, tdk, tdv, p, causal, dropout, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -57,9 +57,11 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 cudaError_t launch_bwd_pre(const void* O, const void* dO, const float* LSE, float* lse2,
                            float* Drow, float* dq_acc, int BH, int N, int Npad, int d,
                            cudaStream_t stream);
+// tdk / tdv: maps over the dK / dV outputs, written with TMA stores.
 cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdParams& p, int d, bool causal,
-                            bool dropout, cudaStream_t stream);
+                            const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                            const BwdParams& p, int d, bool causal, bool dropout,
+                            cudaStream_t stream);
 cudaError_t launch_bwd_dq_convert(void* dQ, const float* dq_acc, int BH, int N, int Npad, int d,
                                   float scale, cudaStream_t stream);
 
