@@ -20,74 +20,97 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// One warp per padded row.  Rows >= N (and rows whose LSE is -inf, which have
-// no valid key) get lse2 = +inf so that the main kernel's P = exp2(s - lse2)
-// is exactly 0 there.
+// D_i = dO_i . O_i and lse2_i = LSE_i log2(e) for every padded row, and the
+// row's fp32 dQ accumulator cleared.  Rows >= N (and rows whose LSE is -inf,
+// which have no valid key) get lse2 = +inf so that the main kernel's
+// P = exp2(s - lse2) is exactly 0 there.
+//
+// Bandwidth layout: a row is handled by D / 8 consecutive threads, each
+// loading 16 bytes (8 bf16) of O and of dO and clearing 32 bytes of the
+// accumulator; every thread covers kPreRows rows, whose loads are all issued
+// before the first product so that enough bytes are in flight.
+constexpr int kPreThreads = 256;
+constexpr int kPreRows = 2;
+
 template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ O,
-                                                      const __nv_bfloat16* __restrict__ dO,
-                                                      const float* __restrict__ LSE,
-                                                      float* __restrict__ lse2,
-                                                      float* __restrict__ Drow,
-                                                      float* __restrict__ dq_acc, int BH, int N,
-                                                      int Npad) {
-    const int lane = threadIdx.x & 31;
-    const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-    if (prow >= static_cast<long long>(BH) * Npad) return;
-    const int bh = static_cast<int>(prow / Npad);
-    const int row = static_cast<int>(prow % Npad);
-    constexpr int PER = D / 32;   // elements per lane
-    float acc = 0.f;
-    if (row < N) {
-        const size_t base = (static_cast<size_t>(bh) * N + row) * D + lane * PER;
-        if constexpr (PER == 4) {
-            const uint2 a = *reinterpret_cast<const uint2*>(O + base);
-            const uint2 g = *reinterpret_cast<const uint2*>(dO + base);
-            acc = bf16lo_to_f32(a.x) * bf16lo_to_f32(g.x) + bf16hi_to_f32(a.x) * bf16hi_to_f32(g.x) +
-                  bf16lo_to_f32(a.y) * bf16lo_to_f32(g.y) + bf16hi_to_f32(a.y) * bf16hi_to_f32(g.y);
-        } else {
-            const uint32_t a = *reinterpret_cast<const uint32_t*>(O + base);
-            const uint32_t g = *reinterpret_cast<const uint32_t*>(dO + base);
-            acc = bf16lo_to_f32(a) * bf16lo_to_f32(g) + bf16hi_to_f32(a) * bf16hi_to_f32(g);
+__global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const __nv_bfloat16* __restrict__ O,
+                                                              const __nv_bfloat16* __restrict__ dO,
+                                                              const float* __restrict__ LSE,
+                                                              float* __restrict__ lse2,
+                                                              float* __restrict__ Drow,
+                                                              float* __restrict__ dq_acc, int BH,
+                                                              int N, int Npad) {
+    constexpr int TPR = D / 8;                          // threads per row
+    constexpr int ROWS_PER_PASS = kPreThreads / TPR;    // rows one pass of the block covers
+    const int sub = threadIdx.x % TPR;                  // 8-element slice of the row
+    const long long total = static_cast<long long>(BH) * Npad;
+    long long prow[kPreRows];
+    uint4 a[kPreRows], g[kPreRows];
+#pragma unroll
+    for (int k = 0; k < kPreRows; ++k) {
+        prow[k] = (static_cast<long long>(blockIdx.x) * kPreRows + k) * ROWS_PER_PASS + threadIdx.x / TPR;
+        a[k] = make_uint4(0, 0, 0, 0);
+        g[k] = make_uint4(0, 0, 0, 0);
+        if (prow[k] < total) {
+            const int bh = static_cast<int>(prow[k] / Npad);
+            const int row = static_cast<int>(prow[k] % Npad);
+            if (row < N) {
+                const size_t off = (static_cast<size_t>(bh) * N + row) * D + 8 * sub;
+                a[k] = *reinterpret_cast<const uint4*>(O + off);
+                g[k] = *reinterpret_cast<const uint4*>(dO + off);
+            }
         }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    float* qa = dq_acc + static_cast<size_t>(prow) * D + lane * PER;
-    if constexpr (PER == 4) {
-        *reinterpret_cast<float4*>(qa) = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-        *reinterpret_cast<float2*>(qa) = make_float2(0.f, 0.f);
-    }
-    if (lane == 0) {
-        float l2 = INFINITY;
-        if (row < N) {
-            const float lse = LSE[static_cast<size_t>(bh) * N + row];
-            if (lse != -INFINITY) l2 = lse * kLog2e;
+    for (int k = 0; k < kPreRows; ++k) {
+        const uint32_t av[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
+        const uint32_t gv[4] = {g[k].x, g[k].y, g[k].z, g[k].w};
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            acc += bf16lo_to_f32(av[e]) * bf16lo_to_f32(gv[e]) + bf16hi_to_f32(av[e]) * bf16hi_to_f32(gv[e]);
+#pragma unroll
+        for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (prow[k] >= total) continue;
+        float4* qa = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(prow[k]) * D + 8 * sub);
+        qa[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        qa[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (sub == 0) {
+            const int bh = static_cast<int>(prow[k] / Npad);
+            const int row = static_cast<int>(prow[k] % Npad);
+            float l2 = INFINITY;
+            if (row < N) {
+                const float lse = LSE[static_cast<size_t>(bh) * N + row];
+                if (lse != -INFINITY) l2 = lse * kLog2e;
+            }
+            lse2[prow[k]] = l2;
+            Drow[prow[k]] = acc;
         }
-        lse2[prow] = l2;
-        Drow[prow] = acc;
     }
 }
 
-// dQ = scale * acc for valid rows; 4 elements per thread.
+// dQ = scale * acc for valid rows; 8 elements (two 16-byte loads, one 16-byte
+// store) per thread.
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(__nv_bfloat16* __restrict__ dQ,
                                                              const float* __restrict__ dq_acc,
-                                                             long long n4, int N, int Npad, int D,
+                                                             long long n8, int N, int Npad, int D,
                                                              float scale) {
-    const long long i4 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i4 >= n4) return;
-    const long long e = i4 * 4;                 // element index in [BH][N][D]
+    const long long i8 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i8 >= n8) return;
+    const long long e = i8 * 8;                 // element index in [BH][N][D]
     const long long rowg = e / D;               // bh * N + row
     const int c = static_cast<int>(e % D);
     const long long bh = rowg / N;
     const int row = static_cast<int>(rowg % N);
-    const float4 a = *reinterpret_cast<const float4*>(
+    const float4* src = reinterpret_cast<const float4*>(
         dq_acc + (static_cast<size_t>(bh) * Npad + row) * D + c);
-    uint2 out;
-    out.x = pack_bf16x2(a.x * scale, a.y * scale);
-    out.y = pack_bf16x2(a.z * scale, a.w * scale);
-    *reinterpret_cast<uint2*>(dQ + e) = out;
+    const float4 x = src[0], y = src[1];
+    uint4 out;
+    out.x = pack_bf16x2(x.x * scale, x.y * scale);
+    out.y = pack_bf16x2(x.z * scale, x.w * scale);
+    out.z = pack_bf16x2(y.x * scale, y.y * scale);
+    out.w = pack_bf16x2(y.z * scale, y.w * scale);
+    *reinterpret_cast<uint4*>(dQ + e) = out;
 }
 
 // ---------------------------------------------------------------------------
@@ -737,15 +760,16 @@ cudaError_t launch_bwd_pre(const void* O, const void* dO, const float* LSE, floa
                            float* Drow, float* dq_acc, int BH, int N, int Npad, int d,
                            cudaStream_t stream) {
     const long long rows = static_cast<long long>(BH) * Npad;
-    const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+    const int rows_per_block = (kPreThreads / (d / 8)) * kPreRows;
+    const unsigned grid = static_cast<unsigned>((rows + rows_per_block - 1) / rows_per_block);
     if (d == 64)
-        bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(O),
-                                                     static_cast<const __nv_bfloat16*>(dO), LSE,
-                                                     lse2, Drow, dq_acc, BH, N, Npad);
+        bwd_pre_kernel<64><<<grid, kPreThreads, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, lse2,
+            Drow, dq_acc, BH, N, Npad);
     else if (d == 128)
-        bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(O),
-                                                      static_cast<const __nv_bfloat16*>(dO), LSE,
-                                                      lse2, Drow, dq_acc, BH, N, Npad);
+        bwd_pre_kernel<128><<<grid, kPreThreads, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, lse2,
+            Drow, dq_acc, BH, N, Npad);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();
@@ -753,9 +777,9 @@ cudaError_t launch_bwd_pre(const void* O, const void* dO, const float* LSE, floa
 
 cudaError_t launch_bwd_dq_convert(void* dQ, const float* dq_acc, int BH, int N, int Npad, int d,
                                   float scale, cudaStream_t stream) {
-    const long long n4 = static_cast<long long>(BH) * N * d / 4;
-    const unsigned grid = static_cast<unsigned>((n4 + 255) / 256);
-    bwd_dq_convert_kernel<<<grid, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(dQ), dq_acc, n4,
+    const long long n8 = static_cast<long long>(BH) * N * d / 8;
+    const unsigned grid = static_cast<unsigned>((n8 + 255) / 256);
+    bwd_dq_convert_kernel<<<grid, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(dQ), dq_acc, n8,
                                                     N, Npad, d, scale);
     return cudaGetLastError();
 }
