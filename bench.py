@@ -265,13 +265,16 @@ def run_ours(args, w: Workload):
     ea.library()
 
     inp = make_workload_inputs(args.workload)
-    q, k, v, do = (t.to(dev) for t in (inp.q, inp.k, inp.v, inp.do))
+    q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
+    bwd = w.backward   # forward-only workloads time the forward alone
+    do = inp.do.to(dev) if bwd else None
     kl = inp.key_lens.to(dev) if inp.key_lens is not None else None
     B, H, N, d = q.shape
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
-    ws = torch.empty(ea.attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    if bwd:
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        ws = torch.empty(ea.attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     kw = dict(causal=w.causal, key_lens=kl, dropout_p=inp.dropout_p, seed=inp.seed,
               scale=inp.scale)
@@ -282,15 +285,25 @@ def run_ours(args, w: Workload):
         ea.attn_fwd(q, k, v, out=o, lse=lse, dev_status=status, **kw)
         if evs:
             evs[1].record()
-        ea.attn_bwd_preprocess(o, do, lse, ws)
+        if bwd:
+            ea.attn_bwd_preprocess(o, do, lse, ws)
         if evs:
             evs[2].record()
-        ea.attn_bwd_main(q, k, v, do, dk, dv, ws, dev_status=status, **kw)
+        if bwd:
+            ea.attn_bwd_main(q, k, v, do, dk, dv, ws, dev_status=status, **kw)
         if evs:
             evs[3].record()
-        ea.attn_bwd_dq_convert(dq, ws, scale=inp.scale)
+        if bwd:
+            ea.attn_bwd_dq_convert(dq, ws, scale=inp.scale)
         if evs:
             evs[4].record()
+
+    # Inputs that fit in L2 would be served from it on every step; then L2 is
+    # flushed (a 256 MiB write) before each step, outside the per-stage
+    # events, and the step time is the sum of the stage times.
+    in_bytes = (4 if bwd else 3) * q.numel() * q.element_size()
+    flush = in_bytes <= L2_BYTES
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush else None
 
     for _ in range(args.warmup):
         step()
@@ -308,6 +321,8 @@ def run_ours(args, w: Workload):
         sampler.start()
     start.record()
     for s in range(args.steps):
+        if flush:
+            flush_buf.zero_()
         step(evs[s])
     end.record()
     torch.cuda.synchronize()
@@ -319,20 +334,22 @@ def run_ours(args, w: Workload):
 
     elapsed_ms = start.elapsed_time(end)
     per = [[evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps)] for i in range(4)]
+    if flush:   # the flushes are not part of the step
+        elapsed_ms = sum(evs[s][0].elapsed_time(evs[s][4]) for s in range(args.steps))
     if world > 1:
         t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
 
-    flops_fwd, flops_bwd = w.flops_fwd(), w.flops_bwd()
+    flops_fwd, flops_bwd = w.flops_fwd(), (w.flops_bwd() if bwd else 0.0)
     flops_step = flops_fwd + flops_bwd
     value = world * flops_step * args.steps / (elapsed_ms * 1e-3) / 1e12
     fwd_ms, pre_ms, main_ms, conv_ms = (statistics.mean(x) for x in per)
     peak, peak_sus, hbm, peak_src = load_peaks()
     fwd_tf = flops_fwd / (fwd_ms * 1e-3) / 1e12
-    bwd_tf = flops_bwd / ((pre_ms + main_ms + conv_ms) * 1e-3) / 1e12
-    main_tf = flops_bwd / (main_ms * 1e-3) / 1e12
-    if main_ms >= fwd_ms:
+    bwd_tf = flops_bwd / ((pre_ms + main_ms + conv_ms) * 1e-3) / 1e12 if bwd else None
+    main_tf = flops_bwd / (main_ms * 1e-3) / 1e12 if bwd else None
+    if bwd and main_ms >= fwd_ms:
         dom, dom_tf, dom_ms = "attn_bwd_kernel", main_tf, main_ms
     else:
         dom, dom_tf, dom_ms = "attn_fwd_kernel", fwd_tf, fwd_ms
@@ -348,7 +365,8 @@ def run_ours(args, w: Workload):
     # ---- end to end through the public API with pinned host buffers ----
     e2e = None
     if args.e2e_steps > 0:
-        hq, hk, hv, hdo = (t.pin_memory() for t in (inp.q, inp.k, inp.v, inp.do))
+        hq, hk, hv = (t.pin_memory() for t in (inp.q, inp.k, inp.v))
+        hdo = inp.do.pin_memory() if bwd else None
         ho, hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(4))
         s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -356,13 +374,16 @@ def run_ours(args, w: Workload):
             q.copy_(hq, non_blocking=True)
             k.copy_(hk, non_blocking=True)
             v.copy_(hv, non_blocking=True)
-            do.copy_(hdo, non_blocking=True)
+            if bwd:
+                do.copy_(hdo, non_blocking=True)
             ea.attn_fwd(q, k, v, out=o, lse=lse, **kw)
-            ea.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
+            if bwd:
+                ea.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
             ho.copy_(o, non_blocking=True)
-            hdq.copy_(dq, non_blocking=True)
-            hdk.copy_(dk, non_blocking=True)
-            hdv.copy_(dv, non_blocking=True)
+            if bwd:
+                hdq.copy_(dq, non_blocking=True)
+                hdk.copy_(dk, non_blocking=True)
+                hdv.copy_(dv, non_blocking=True)
 
         for _ in range(2):
             e2e_step()
@@ -375,30 +396,34 @@ def run_ours(args, w: Workload):
         e_ms = s_ev.elapsed_time(e_ev)
         nbytes = q.numel() * q.element_size()
         e2e = {"value": flops_step * args.e2e_steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 4 * nbytes,
+               "h2d_bytes_per_step": (4 if bwd else 3) * nbytes,
+               "d2h_bytes_per_step": (4 if bwd else 1) * nbytes,
                "ms_per_step": e_ms / args.e2e_steps}
 
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and bwd:   # the sample is forward+backward
         cpu = cpu_baseline(inp, w, target_s=args.cpu_seconds)
 
-    in_bytes = 4 * q.numel() * q.element_size()
+    l2_note = (f"inputs {in_bytes / 2**20:.0f} MiB <= L2: L2 flushed (256 MiB write) before every step"
+               if flush else f"inputs {in_bytes / 2**20:.0f} MiB > L2 {L2_BYTES / 2**20:.0f} MiB, no flush")
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "tf32",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                   "causal": w.causal, "dropout_p": w.dropout_p, "passes": "fwd+bwd",
+                   "causal": w.causal, "dropout_p": w.dropout_p,
+                   "passes": "fwd+bwd" if bwd else "fwd",
                    "global_batch": world * w.B, "seq_len": w.N,
                    "parallelism": f"replicas x{world} (heads independent)",
-                   "l2": f"inputs {in_bytes / 2**20:.0f} MiB > L2 {L2_BYTES / 2**20:.0f} MiB, no flush"},
+                   "l2": l2_note},
         "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "fwd_frac_peak": fwd_tf / peak,
-        "bwd_frac_peak": bwd_tf / peak, "peak_tflops": peak,
+        "bwd_frac_peak": bwd_tf / peak if bwd else None, "peak_tflops": peak,
         "kernel_ms": {"attn_fwd_kernel": fwd_ms, "bwd_pre_kernel": pre_ms,
                       "attn_bwd_kernel": main_ms, "bwd_dq_convert_kernel": conv_ms},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": 4 * args.steps, "clocks": clocks,
+        "gpu_launches": (4 if bwd else 1) * args.steps, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
