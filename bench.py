@@ -265,6 +265,11 @@ def run_ours(args, w: Workload):
     ea.library()
 
     inp = make_workload_inputs(args.workload)
+    if args.dtype == "fp16":   # the same draws stored as IEEE half
+        for name in ("q", "k", "v", "do"):
+            t = getattr(inp, name)
+            if t is not None:
+                setattr(inp, name, t.to(torch.float32).to(torch.float16))
     q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
     bwd = w.backward   # forward-only workloads time the forward alone
     do = inp.do.to(dev) if bwd else None
@@ -410,7 +415,7 @@ def run_ours(args, w: Workload):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if w.dtype == "bf16" else "tf32",
+        "dtype": args.dtype if args.dtype != "default" else ("bf16" if w.dtype == "bf16" else "tf32"),
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                    "causal": w.causal, "dropout_p": w.dropout_p,
@@ -438,6 +443,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, help="1-based workload index")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--dtype", choices=["default", "fp16"], default="default",
+                    help="fp16: store the workload's inputs as IEEE half (16-bit workloads only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget-s", type=float, default=120.0)

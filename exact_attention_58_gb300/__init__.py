@@ -42,7 +42,7 @@ STATUS = {
     5: "ATTN_ERR_CUDA",
     6: "ATTN_ERR_DEVICE_TIMEOUT",
 }
-_DTYPE = {torch.bfloat16: 0, torch.float32: 1}
+_DTYPE = {torch.bfloat16: 0, torch.float32: 1, torch.float16: 2}
 
 _lock = threading.Lock()
 _lib = None

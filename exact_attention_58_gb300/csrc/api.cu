@@ -33,7 +33,8 @@ int npad_of(int N) { return ((N + kTileRows - 1) / kTileRows) * kTileRows; }
 // Checks shared by every entry point that takes a shape.
 attn_status check_shape(int B, int H, int N, int d, attn_dtype dtype, bool backward) {
     if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
-    if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP32) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP32 && dtype != ATTN_DTYPE_FP16)
+        return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     if (dtype == ATTN_DTYPE_FP32 && (backward || d != 64)) return ATTN_ERR_UNSUPPORTED;
     const long long elems = static_cast<long long>(B) * H * npad_of(N) * d;
@@ -80,7 +81,8 @@ attn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_
 
 }  // namespace
 
-bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, bool fp32, int BH, int N, int d) {
+bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int BH, int N, int d) {
+    const bool fp32 = dtype == ATTN_DTYPE_FP32;
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (enc == nullptr) return false;
     const cuuint64_t es = fp32 ? 4 : 2;
@@ -91,7 +93,10 @@ bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, bool fp32, int BH, int N,
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(kTileRows), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r =
-        enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+        enc(map,
+            fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                 : (dtype == ATTN_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16),
+            3,
             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -114,10 +119,9 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
     if ((st = check_math(scale, dropout_p)) != ATTN_OK) return st;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
         return ATTN_ERR_MISALIGNED;
-    const bool fp32 = dtype == ATTN_DTYPE_FP32;
     CUtensorMap tq, tk, tv;
-    if (!make_tmap_bhnd(&tq, Q, fp32, B * H, N, d) || !make_tmap_bhnd(&tk, K, fp32, B * H, N, d) ||
-        !make_tmap_bhnd(&tv, V, fp32, B * H, N, d))
+    if (!make_tmap_bhnd(&tq, Q, dtype, B * H, N, d) || !make_tmap_bhnd(&tk, K, dtype, B * H, N, d) ||
+        !make_tmap_bhnd(&tv, V, dtype, B * H, N, d))
         return ATTN_ERR_CUDA;
     FwdParams p{};
     p.V = V;
@@ -134,7 +138,7 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
     p.drop_threshold = drop_threshold(dropout_p);
     p.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFu);
     p.seed_hi = static_cast<uint32_t>(seed >> 32);
-    return from_cuda(launch_fwd(tq, tk, tv, p, d, fp32, causal != 0, dropout_p > 0.f,
+    return from_cuda(launch_fwd(tq, tk, tv, p, d, dtype, causal != 0, dropout_p > 0.f,
                                 static_cast<cudaStream_t>(stream)));
 }
 
@@ -153,7 +157,7 @@ attn_status attn_bwd_preprocess(const void* O, const void* dO, const float* LSE,
     if (!aligned16(O) || !aligned16(dO) || !aligned16(LSE)) return ATTN_ERR_MISALIGNED;
     const Workspace w = carve(workspace, B, H, N);
     return from_cuda(launch_bwd_pre(O, dO, LSE, w.lse2, w.Drow, w.dq_acc, B * H, N, npad_of(N),
-                                    d, static_cast<cudaStream_t>(stream)));
+                                    d, dtype == ATTN_DTYPE_FP16, static_cast<cudaStream_t>(stream)));
 }
 
 attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dK,
@@ -170,9 +174,9 @@ attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const voi
         !aligned16(dV))
         return ATTN_ERR_MISALIGNED;
     CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-    if (!make_tmap_bhnd(&tq, Q, false, B * H, N, d) || !make_tmap_bhnd(&tk, K, false, B * H, N, d) ||
-        !make_tmap_bhnd(&tv, V, false, B * H, N, d) || !make_tmap_bhnd(&tdo, dO, false, B * H, N, d) ||
-        !make_tmap_bhnd(&tdk, dK, false, B * H, N, d) || !make_tmap_bhnd(&tdv, dV, false, B * H, N, d))
+    if (!make_tmap_bhnd(&tq, Q, dtype, B * H, N, d) || !make_tmap_bhnd(&tk, K, dtype, B * H, N, d) ||
+        !make_tmap_bhnd(&tv, V, dtype, B * H, N, d) || !make_tmap_bhnd(&tdo, dO, dtype, B * H, N, d) ||
+        !make_tmap_bhnd(&tdk, dK, dtype, B * H, N, d) || !make_tmap_bhnd(&tdv, dV, dtype, B * H, N, d))
         return ATTN_ERR_CUDA;
     const Workspace w = carve(workspace, B, H, N);
     BwdParams p{};
@@ -194,7 +198,8 @@ attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const voi
     p.drop_threshold = drop_threshold(dropout_p);
     p.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFu);
     p.seed_hi = static_cast<uint32_t>(seed >> 32);
-    return from_cuda(launch_bwd_main(tq, tk, tv, tdo, tdk, tdv, p, d, causal != 0, dropout_p > 0.f,
+    return from_cuda(launch_bwd_main(tq, tk, tv, tdo, tdk, tdv, p, d, dtype == ATTN_DTYPE_FP16,
+                                     causal != 0, dropout_p > 0.f,
                                      static_cast<cudaStream_t>(stream)));
 }
 
@@ -208,7 +213,8 @@ attn_status attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, attn_dtype
     if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != ATTN_OK) return st;
     if (!aligned16(dQ)) return ATTN_ERR_MISALIGNED;
     const Workspace w = carve(const_cast<void*>(workspace), B, H, N);
-    return from_cuda(launch_bwd_dq_convert(dQ, w.dq_acc, B * H, N, npad_of(N), d, scale,
+    return from_cuda(launch_bwd_dq_convert(dQ, w.dq_acc, B * H, N, npad_of(N), d,
+                                           dtype == ATTN_DTYPE_FP16, scale,
                                            static_cast<cudaStream_t>(stream)));
 }
 

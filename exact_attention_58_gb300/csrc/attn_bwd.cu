@@ -26,15 +26,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 // P = exp2(s - lse2) is exactly 0 there.
 //
 // Bandwidth layout: a row is handled by D / 8 consecutive threads, each
-// loading 16 bytes (8 bf16) of O and of dO and clearing 32 bytes of the
+// loading 16 bytes (8 elements) of O and of dO and clearing 32 bytes of the
 // accumulator; every thread covers kPreRows rows, whose loads are all issued
 // before the first product so that enough bytes are in flight.
 constexpr int kPreThreads = 256;
 constexpr int kPreRows = 2;
 
-template <int D>
-__global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const __nv_bfloat16* __restrict__ O,
-                                                              const __nv_bfloat16* __restrict__ dO,
+template <int D, bool kF16>
+__global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const uint16_t* __restrict__ O,
+                                                              const uint16_t* __restrict__ dO,
                                                               const float* __restrict__ LSE,
                                                               float* __restrict__ lse2,
                                                               float* __restrict__ Drow,
@@ -68,7 +68,8 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const __nv_bfloat1
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            acc += bf16lo_to_f32(av[e]) * bf16lo_to_f32(gv[e]) + bf16hi_to_f32(av[e]) * bf16hi_to_f32(gv[e]);
+            acc += h2lo_to_f32<kF16>(av[e]) * h2lo_to_f32<kF16>(gv[e]) +
+                   h2hi_to_f32<kF16>(av[e]) * h2hi_to_f32<kF16>(gv[e]);
 #pragma unroll
         for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (prow[k] >= total) continue;
@@ -91,7 +92,8 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const __nv_bfloat1
 
 // dQ = scale * acc for valid rows; 8 elements (two 16-byte loads, one 16-byte
 // store) per thread.
-__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(__nv_bfloat16* __restrict__ dQ,
+template <bool kF16>
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(uint16_t* __restrict__ dQ,
                                                              const float* __restrict__ dq_acc,
                                                              long long n8, int N, int Npad, int D,
                                                              float scale) {
@@ -106,10 +108,10 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(__nv_bfloat16* __re
         dq_acc + (static_cast<size_t>(bh) * Npad + row) * D + c);
     const float4 x = src[0], y = src[1];
     uint4 out;
-    out.x = pack_bf16x2(x.x * scale, x.y * scale);
-    out.y = pack_bf16x2(x.z * scale, x.w * scale);
-    out.z = pack_bf16x2(y.x * scale, y.y * scale);
-    out.w = pack_bf16x2(y.z * scale, y.w * scale);
+    out.x = pack_h2<kF16>(x.x * scale, x.y * scale);
+    out.y = pack_h2<kF16>(x.z * scale, x.w * scale);
+    out.z = pack_h2<kF16>(y.x * scale, y.y * scale);
+    out.w = pack_h2<kF16>(y.z * scale, y.w * scale);
     *reinterpret_cast<uint4*>(dQ + e) = out;
 }
 
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(__nv_bfloat16* __re
 // of its 64-column half of S.  dS goes to shared memory only: it is the
 // MN-major operand of the dQ product and, read as K-major with keys as rows,
 // the A operand of dK += dS^T Q.
-template <int D>
+template <int D, bool kF16>
 struct BwdCfg {
     static constexpr int THREADS = 448;
     static constexpr int ROWB = D * 2;
@@ -177,16 +179,17 @@ struct BwdCfg {
     // dQ, fp32: its own columns for d = 64; for d = 128 it reuses the dP
     // columns, which are free once P and dS have been built.
     static constexpr uint32_t C_DQ = (D == 64) ? 2 * D + 256 : C_DP;
-    static constexpr uint32_t IDESC_SDP = idesc_f32acc(128, 128, false, false, false);
-    static constexpr uint32_t IDESC_DP_HALF = idesc_f32acc(128, 64, false, false, false);
-    static constexpr uint32_t IDESC_DKV = idesc_f32acc(128, D, false, false, true);
+    static constexpr uint32_t FMT = fmt16<kF16>();   // every operand has the storage type
+    static constexpr uint32_t IDESC_SDP = idesc_f32acc(128, 128, FMT, false, false);
+    static constexpr uint32_t IDESC_DP_HALF = idesc_f32acc(128, 64, FMT, false, false);
+    static constexpr uint32_t IDESC_DKV = idesc_f32acc(128, D, FMT, false, true);
     // d = 64: dQ = dS K (lanes = queries, N = 64).  d = 128: dQ^T = K^T dS^T
     // (lanes = head-dim columns), one N = 64 product per query half.
-    static constexpr uint32_t IDESC_DQ = idesc_f32acc(128, 64, false, true, true);
+    static constexpr uint32_t IDESC_DQ = idesc_f32acc(128, 64, FMT, true, true);
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <int D, bool kCausal, bool kDropout>
+template <int D, bool kF16, bool kCausal, bool kDropout>
 __global__ void __launch_bounds__(448, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
@@ -194,7 +197,7 @@ __global__ void __launch_bounds__(448, 1)
                     const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdK,
                     const __grid_constant__ CUtensorMap tmdV, const BwdParams p) {
-    using C = BwdCfg<D>;
+    using C = BwdCfg<D, kF16>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -216,9 +219,9 @@ __global__ void __launch_bounds__(448, 1)
     if (k0 >= L) {   // every key of this block is masked: dK = dV = 0
         const int rows = min(kTileRows, N - k0);
         const int n16 = rows * D / 8;   // uint4 per tensor
-        uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dK) + head_off +
+        uint4* dk = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dK) + head_off +
                                              static_cast<size_t>(k0) * D);
-        uint4* dv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dV) + head_off +
+        uint4* dv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dV) + head_off +
                                              static_cast<size_t>(k0) * D);
         for (int x = threadIdx.x; x < n16; x += blockDim.x) {
             dk[x] = make_uint4(0, 0, 0, 0);
@@ -541,7 +544,7 @@ __global__ void __launch_bounds__(448, 1)
                         if constexpr (kDropout)
                             pd[u] = ((keep >> (2 * e + u)) & 1u) ? x * p.drop_scale : 0.f;
                     }
-                    pk[e] = pack_bf16x2(pd[0], pd[1]);
+                    pk[e] = pack_h2<kF16>(pd[0], pd[1]);
                 }
                 tmem_st8(tS + 8 * c, pk);
                 if (c < 3) {
@@ -587,7 +590,7 @@ __global__ void __launch_bounds__(448, 1)
                             dp = ((keepw[c] >> (2 * e + u)) & 1u) ? dp * p.drop_scale : 0.f;
                         ds[u] = pr[col] * (dp - dv[2 * e + u]);
                     }
-                    dk[e] = pack_bf16x2(ds[0], ds[1]);
+                    dk[e] = pack_h2<kF16>(ds[0], ds[1]);
                 }
                 // dS (bf16) into shared memory: query index innermost (one
                 // 64-query block per half), 128-byte swizzle.  bar_dP of this
@@ -633,7 +636,7 @@ __global__ void __launch_bounds__(448, 1)
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        w[e] = pack_bf16x2(__uint_as_float(a[8 * q4 + 2 * e]) * mul,
+                        w[e] = pack_h2<kF16>(__uint_as_float(a[8 * q4 + 2 * e]) * mul,
                                            __uint_as_float(a[8 * q4 + 2 * e + 1]) * mul);
                     const int chunk = (4 * (c & 1) + q4) ^ (r & 7);
                     *reinterpret_cast<uint4*>(rowp + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -726,12 +729,12 @@ __global__ void __launch_bounds__(448, 1)
         atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_DEVICE_TIMEOUT));
 }
 
-template <int D, bool kCausal, bool kDropout>
+template <int D, bool kF16, bool kCausal, bool kDropout>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                          const BwdParams& p, cudaStream_t stream) {
-    using C = BwdCfg<D>;
-    auto kern = attn_bwd_kernel<D, kCausal, kDropout>;
+    using C = BwdCfg<D, kF16>;
+    auto kern = attn_bwd_kernel<D, kF16, kCausal, kDropout>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -743,53 +746,68 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool kF16>
 cudaError_t dispatch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                          const BwdParams& p, bool causal, bool dropout, cudaStream_t s) {
     if (causal)
-        return dropout ? launch_bwd_t<D, true, true>(tq, tk, tv, tdo, tdk, tdv, p, s)
-                       : launch_bwd_t<D, true, false>(tq, tk, tv, tdo, tdk, tdv, p, s);
-    return dropout ? launch_bwd_t<D, false, true>(tq, tk, tv, tdo, tdk, tdv, p, s)
-                   : launch_bwd_t<D, false, false>(tq, tk, tv, tdo, tdk, tdv, p, s);
+        return dropout ? launch_bwd_t<D, kF16, true, true>(tq, tk, tv, tdo, tdk, tdv, p, s)
+                       : launch_bwd_t<D, kF16, true, false>(tq, tk, tv, tdo, tdk, tdv, p, s);
+    return dropout ? launch_bwd_t<D, kF16, false, true>(tq, tk, tv, tdo, tdk, tdv, p, s)
+                   : launch_bwd_t<D, kF16, false, false>(tq, tk, tv, tdo, tdk, tdv, p, s);
+}
+
+template <int D, bool kF16>
+void launch_pre_t(unsigned grid, const void* O, const void* dO, const float* LSE, float* lse2,
+                  float* Drow, float* dq_acc, int BH, int N, int Npad, cudaStream_t stream) {
+    bwd_pre_kernel<D, kF16><<<grid, kPreThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), LSE, lse2, Drow, dq_acc,
+        BH, N, Npad);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_pre(const void* O, const void* dO, const float* LSE, float* lse2,
-                           float* Drow, float* dq_acc, int BH, int N, int Npad, int d,
+                           float* Drow, float* dq_acc, int BH, int N, int Npad, int d, bool f16,
                            cudaStream_t stream) {
     const long long rows = static_cast<long long>(BH) * Npad;
     const int rows_per_block = (kPreThreads / (d / 8)) * kPreRows;
     const unsigned grid = static_cast<unsigned>((rows + rows_per_block - 1) / rows_per_block);
-    if (d == 64)
-        bwd_pre_kernel<64><<<grid, kPreThreads, 0, stream>>>(
-            static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, lse2,
-            Drow, dq_acc, BH, N, Npad);
-    else if (d == 128)
-        bwd_pre_kernel<128><<<grid, kPreThreads, 0, stream>>>(
-            static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, lse2,
-            Drow, dq_acc, BH, N, Npad);
-    else
+    if (d == 64) {
+        if (f16) launch_pre_t<64, true>(grid, O, dO, LSE, lse2, Drow, dq_acc, BH, N, Npad, stream);
+        else launch_pre_t<64, false>(grid, O, dO, LSE, lse2, Drow, dq_acc, BH, N, Npad, stream);
+    } else if (d == 128) {
+        if (f16) launch_pre_t<128, true>(grid, O, dO, LSE, lse2, Drow, dq_acc, BH, N, Npad, stream);
+        else launch_pre_t<128, false>(grid, O, dO, LSE, lse2, Drow, dq_acc, BH, N, Npad, stream);
+    } else {
         return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq_convert(void* dQ, const float* dq_acc, int BH, int N, int Npad, int d,
-                                  float scale, cudaStream_t stream) {
+                                  bool f16, float scale, cudaStream_t stream) {
     const long long n8 = static_cast<long long>(BH) * N * d / 8;
     const unsigned grid = static_cast<unsigned>((n8 + 255) / 256);
-    bwd_dq_convert_kernel<<<grid, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(dQ), dq_acc, n8,
-                                                    N, Npad, d, scale);
+    if (f16)
+        bwd_dq_convert_kernel<true><<<grid, 256, 0, stream>>>(static_cast<uint16_t*>(dQ), dq_acc, n8,
+                                                              N, Npad, d, scale);
+    else
+        bwd_dq_convert_kernel<false><<<grid, 256, 0, stream>>>(static_cast<uint16_t*>(dQ), dq_acc, n8,
+                                                               N, Npad, d, scale);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                            const BwdParams& p, int d, bool causal, bool dropout,
+                            const BwdParams& p, int d, bool f16, bool causal, bool dropout,
                             cudaStream_t stream) {
-    if (d == 64) return dispatch_bwd<64>(tq, tk, tv, tdo, tdk, tdv, p, causal, dropout, stream);
-    if (d == 128) return dispatch_bwd<128>(tq, tk, tv, tdo, tdk, tdv, p, causal, dropout, stream);
+    if (d == 64)
+        return f16 ? dispatch_bwd<64, true>(tq, tk, tv, tdo, tdk, tdv, p, causal, dropout, stream)
+                   : dispatch_bwd<64, false>(tq, tk, tv, tdo, tdk, tdv, p, causal, dropout, stream);
+    if (d == 128)
+        return f16 ? dispatch_bwd<128, true>(tq, tk, tv, tdo, tdk, tdv, p, causal, dropout, stream)
+                   : dispatch_bwd<128, false>(tq, tk, tv, tdo, tdk, tdv, p, causal, dropout, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -38,7 +38,7 @@
 namespace gbattn {
 namespace {
 
-template <int D, bool kTF32>
+template <int D, bool kTF32, bool kF16>
 struct FwdCfg {
     static constexpr int ES = kTF32 ? 4 : 2;               // element bytes
     static constexpr int ROWB = D * ES;                    // bytes per row
@@ -51,8 +51,9 @@ struct FwdCfg {
     static constexpr int QK_STEPS = ROWB / 32;             // MMAs per S tile
     static constexpr int PV_STEPS = kTileRows / KSTEP;     // MMAs per P V
     static constexpr int SMEM = (2 + NSLOT) * TILE + 1024 /*barriers*/ + 1024 /*align*/;
-    static constexpr uint32_t IDESC_QK = idesc_f32acc(128, 128, kTF32, false, false);
-    static constexpr uint32_t IDESC_PV = idesc_f32acc(128, D, kTF32, false, !kTF32);
+    static constexpr uint32_t FMT = kTF32 ? kFmtTF32 : fmt16<kF16>();
+    static constexpr uint32_t IDESC_QK = idesc_f32acc(128, 128, FMT, false, false);
+    static constexpr uint32_t IDESC_PV = idesc_f32acc(128, D, FMT, false, !kTF32);
     static_assert(ROWB == 128 || ROWB == 256, "tile rows must be 128 or 256 bytes");
 };
 
@@ -87,12 +88,12 @@ __device__ __forceinline__ void store_v_transposed(const float* __restrict__ Vh,
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <int D, bool kTF32, bool kCausal, bool kDropout>
+template <int D, bool kTF32, bool kF16, bool kCausal, bool kDropout>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-    using C = FwdCfg<D, kTF32>;
+    using C = FwdCfg<D, kTF32, kF16>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -420,9 +421,9 @@ __global__ void __launch_bounds__(320, 1)
                                                      __uint_as_float(sv[4 * g + 2 * e + 1])),
                                              sc2, nm2),
                                       x0, x1);
-                            uint32_t u = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+                            uint32_t u = pack_h2<kF16>(ex2_approx(x0), ex2_approx(x1));
                             acc2[(2 * g + e) & 3] = f2_add(
-                                acc2[(2 * g + e) & 3], f2_pack(bf16lo_to_f32(u), bf16hi_to_f32(u)));
+                                acc2[(2 * g + e) & 3], f2_pack(h2lo_to_f32<kF16>(u), h2hi_to_f32<kF16>(u)));
                             if constexpr (kDropout) {
                                 const uint32_t km = ((keep >> (2 * e)) & 1u ? 0x0000FFFFu : 0u) |
                                                     ((keep >> (2 * e + 1)) & 1u ? 0xFFFF0000u : 0u);
@@ -515,14 +516,14 @@ __global__ void __launch_bounds__(320, 1)
                                                  __uint_as_float(o[4 * v + 3]) * inv);
                     } else {
                         uint4* dst = reinterpret_cast<uint4*>(
-                            static_cast<__nv_bfloat16*>(p.O) + row_off + 32 * c);
+                            static_cast<uint16_t*>(p.O) + row_off + 32 * c);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             uint32_t w[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                w[e] = pack_bf16x2(__uint_as_float(o[8 * v + 2 * e]) * inv,
-                                                   __uint_as_float(o[8 * v + 2 * e + 1]) * inv);
+                                w[e] = pack_h2<kF16>(__uint_as_float(o[8 * v + 2 * e]) * inv,
+                                                     __uint_as_float(o[8 * v + 2 * e + 1]) * inv);
                             dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     }
@@ -543,11 +544,11 @@ __global__ void __launch_bounds__(320, 1)
         atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_DEVICE_TIMEOUT));
 }
 
-template <int D, bool kTF32, bool kCausal, bool kDropout>
+template <int D, bool kTF32, bool kF16, bool kCausal, bool kDropout>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const FwdParams& p, cudaStream_t stream) {
-    using C = FwdCfg<D, kTF32>;
-    auto kern = attn_fwd_kernel<D, kTF32, kCausal, kDropout>;
+    using C = FwdCfg<D, kTF32, kF16>;
+    auto kern = attn_fwd_kernel<D, kTF32, kF16, kCausal, kDropout>;
     static bool configured = false;   // benign race: the attribute call is idempotent
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -559,27 +560,34 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     return cudaGetLastError();
 }
 
-template <int D, bool kTF32>
+template <int D, bool kTF32, bool kF16>
 cudaError_t dispatch_mask(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const FwdParams& p, bool causal, bool dropout, cudaStream_t s) {
     if (causal)
-        return dropout ? launch_fwd_t<D, kTF32, true, true>(tq, tk, tv, p, s)
-                       : launch_fwd_t<D, kTF32, true, false>(tq, tk, tv, p, s);
-    return dropout ? launch_fwd_t<D, kTF32, false, true>(tq, tk, tv, p, s)
-                   : launch_fwd_t<D, kTF32, false, false>(tq, tk, tv, p, s);
+        return dropout ? launch_fwd_t<D, kTF32, kF16, true, true>(tq, tk, tv, p, s)
+                       : launch_fwd_t<D, kTF32, kF16, true, false>(tq, tk, tv, p, s);
+    return dropout ? launch_fwd_t<D, kTF32, kF16, false, true>(tq, tk, tv, p, s)
+                   : launch_fwd_t<D, kTF32, kF16, false, false>(tq, tk, tv, p, s);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int d, bool fp32, bool causal, bool dropout,
+                       const FwdParams& p, int d, attn_dtype dtype, bool causal, bool dropout,
                        cudaStream_t stream) {
-    if (fp32) {
-        if (d == 64) return dispatch_mask<64, true>(tq, tk, tv, p, causal, dropout, stream);
-        return cudaErrorInvalidValue;
+    switch (dtype) {
+        case ATTN_DTYPE_FP32:
+            if (d == 64) return dispatch_mask<64, true, false>(tq, tk, tv, p, causal, dropout, stream);
+            return cudaErrorInvalidValue;
+        case ATTN_DTYPE_BF16:
+            if (d == 64) return dispatch_mask<64, false, false>(tq, tk, tv, p, causal, dropout, stream);
+            if (d == 128) return dispatch_mask<128, false, false>(tq, tk, tv, p, causal, dropout, stream);
+            return cudaErrorInvalidValue;
+        case ATTN_DTYPE_FP16:
+            if (d == 64) return dispatch_mask<64, false, true>(tq, tk, tv, p, causal, dropout, stream);
+            if (d == 128) return dispatch_mask<128, false, true>(tq, tk, tv, p, causal, dropout, stream);
+            return cudaErrorInvalidValue;
     }
-    if (d == 64) return dispatch_mask<64, false>(tq, tk, tv, p, causal, dropout, stream);
-    if (d == 128) return dispatch_mask<128, false>(tq, tk, tv, p, causal, dropout, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -46,23 +46,24 @@ struct BwdParams {
 
 // Tensor map over a contiguous [B*H][N][d] array, 128-row boxes of 128 bytes
 // along d, 128-byte swizzle.  Returns false if the driver rejected it.
-bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, bool fp32, int BH, int N, int d);
+bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int BH, int N, int d);
 
 // Forward launch (validated arguments only).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int d, bool fp32, bool causal, bool dropout,
+                       const FwdParams& p, int d, attn_dtype dtype, bool causal, bool dropout,
                        cudaStream_t stream);
 
 // Backward launches (validated arguments only).
+// f16: the 16-bit tensors are IEEE half (else bf16).
 cudaError_t launch_bwd_pre(const void* O, const void* dO, const float* LSE, float* lse2,
-                           float* Drow, float* dq_acc, int BH, int N, int Npad, int d,
+                           float* Drow, float* dq_acc, int BH, int N, int Npad, int d, bool f16,
                            cudaStream_t stream);
 // tdk / tdv: maps over the dK / dV outputs, written with TMA stores.
 cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                            const BwdParams& p, int d, bool causal, bool dropout,
+                            const BwdParams& p, int d, bool f16, bool causal, bool dropout,
                             cudaStream_t stream);
 cudaError_t launch_bwd_dq_convert(void* dQ, const float* dq_acc, int BH, int N, int Npad, int d,
-                                  float scale, cudaStream_t stream);
+                                  bool f16, float scale, cudaStream_t stream);
 
 }  // namespace gbattn

@@ -346,15 +346,18 @@ __device__ __forceinline__ uint64_t sdesc_adv(uint64_t desc, uint32_t bytes) {
     return desc + static_cast<uint64_t>(bytes >> 4);
 }
 
-// Instruction descriptor for kind::f16 (bf16 operands) and kind::tf32, fp32
-// accumulator, dense: D format (bits 4-5) = f32, A and B formats (bits 7-9,
-// 10-12) = 1 for bf16 / 2 for tf32, A/B major bits 15/16 (0 = K-major,
-// 1 = MN-major), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool tf32, bool a_mn_major,
+// Operand format codes of the instruction descriptor (A and B always share one).
+constexpr uint32_t kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2;
+
+// Instruction descriptor for kind::f16 (f16 or bf16 operands) and kind::tf32,
+// fp32 accumulator, dense: D format (bits 4-5) = f32, A and B formats (bits
+// 7-9, 10-12) = fmt, A/B major bits 15/16 (0 = K-major, 1 = MN-major), N >> 3
+// in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, uint32_t fmt, bool a_mn_major,
                                                     bool b_mn_major) {
-    return (1u << 4) | ((tf32 ? 2u : 1u) << 7) | ((tf32 ? 2u : 1u) << 10) |
-           (static_cast<uint32_t>(a_mn_major) << 15) | (static_cast<uint32_t>(b_mn_major) << 16) |
-           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
+           (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // ---------------------------------------------------------------------------
@@ -422,5 +425,42 @@ __device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_fl
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t v) {
     return __uint_as_float(v & 0xFFFF0000u);
 }
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ float f16lo_to_f32(uint32_t v) {
+    float r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}" : "=f"(r) : "r"(v));
+    return r;
+}
+__device__ __forceinline__ float f16hi_to_f32(uint32_t v) {
+    float r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, hi;\n\t}" : "=f"(r) : "r"(v));
+    return r;
+}
+
+// The 16-bit storage types (bf16 or f16, chosen by kF16): two floats packed
+// with round-to-nearest-even, the low / high half widened back to float, and
+// the tcgen05 operand format code.
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    if constexpr (kF16) return pack_f16x2(lo, hi);
+    else return pack_bf16x2(lo, hi);
+}
+template <bool kF16>
+__device__ __forceinline__ float h2lo_to_f32(uint32_t v) {
+    if constexpr (kF16) return f16lo_to_f32(v);
+    else return bf16lo_to_f32(v);
+}
+template <bool kF16>
+__device__ __forceinline__ float h2hi_to_f32(uint32_t v) {
+    if constexpr (kF16) return f16hi_to_f32(v);
+    else return bf16hi_to_f32(v);
+}
+template <bool kF16>
+constexpr uint32_t fmt16() { return kF16 ? kFmtF16 : kFmtBF16; }
 
 }  // namespace gbattn

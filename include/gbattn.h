@@ -25,8 +25,10 @@
  *  Alignment  Every tensor pointer must be 16-byte aligned
  *             (ATTN_ERR_MISALIGNED otherwise).
  *  Types      ATTN_DTYPE_BF16: bf16 storage, bf16 x bf16 products with fp32
- *             accumulation.  ATTN_DTYPE_FP32: fp32 storage, TF32 products
- *             with fp32 accumulation (forward only, d = 64).
+ *             accumulation.  ATTN_DTYPE_FP16: the same with IEEE half
+ *             storage and f16 x f16 products (P and dS are rounded to f16).
+ *             ATTN_DTYPE_FP32: fp32 storage, TF32 products with fp32
+ *             accumulation (forward only, d = 64).
  *  Shapes     d in {64, 128}; B, H, N >= 1; B*H*N*d < 2^31 elements per
  *             tensor.  Anything else returns ATTN_ERR_UNSUPPORTED or
  *             ATTN_ERR_INVALID_ARG: the library never falls back to another
@@ -80,7 +82,8 @@ typedef enum {
 
 typedef enum {
     ATTN_DTYPE_BF16 = 0,
-    ATTN_DTYPE_FP32 = 1
+    ATTN_DTYPE_FP32 = 1,
+    ATTN_DTYPE_FP16 = 2
 } attn_dtype;
 
 /*
