@@ -55,8 +55,9 @@ def _bind(lib):
     lib.oracle_dropout_mask.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_double, _bp]
     lib.oracle_dropout_mask.restype = None
+    # N, d, scale, causal, window, key_len, p, seed, b, h
     head_common = [ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int,
-                   ctypes.c_double, ctypes.c_uint64, ctypes.c_int, ctypes.c_int]
+                   ctypes.c_int, ctypes.c_double, ctypes.c_uint64, ctypes.c_int, ctypes.c_int]
     lib.oracle_head_fwd.argtypes = [_dp, _dp, _dp, _dp, _dp] + head_common
     lib.oracle_head_fwd.restype = ctypes.c_int
     lib.oracle_head_bwd.argtypes = [_dp] * 8 + head_common
@@ -65,15 +66,17 @@ def _bind(lib):
     lib.oracle_head_fwd_rows.restype = ctypes.c_int
     lib.oracle_head_fwd_tiled.argtypes = [_dp] * 5 + head_common + [ctypes.c_int, ctypes.c_int]
     lib.oracle_head_fwd_tiled.restype = ctypes.c_int
+    # nh, b_idx, h_idx, key_len, N, d, scale, causal, window, p, seed, nthreads
     heads_common = [ctypes.c_int, _ip, _ip, _ip, ctypes.c_int, ctypes.c_int, ctypes.c_double,
-                    ctypes.c_int, ctypes.c_double, ctypes.c_uint64, ctypes.c_int]
+                    ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_uint64, ctypes.c_int]
     lib.oracle_heads_fwd.argtypes = [_dp] * 5 + heads_common
     lib.oracle_heads_fwd.restype = ctypes.c_int
     lib.oracle_heads_bwd.argtypes = [_dp] * 8 + heads_common
     lib.oracle_heads_bwd.restype = ctypes.c_int
     lib.oracle_heads_rows_fwd_bwd.argtypes = (
         [_dp] * 4 + [ctypes.c_int, _ip, _ip, _ip, ctypes.c_int, ctypes.c_int, ctypes.c_double,
-                     ctypes.c_int, ctypes.c_double, ctypes.c_uint64, ctypes.c_int, ctypes.c_int]
+                     ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_uint64, ctypes.c_int,
+                     ctypes.c_int]
         + [_dp] * 5 + [ctypes.c_int])
     lib.oracle_heads_rows_fwd_bwd.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
@@ -141,7 +144,7 @@ def _key_lens(key_lens, B, N):
 
 
 def attn_fwd(Q, K, V, scale=None, causal=False, key_lens=None, dropout_p=0.0, seed=0,
-             nthreads=0, _lib=None):
+             nthreads=0, window=0, _lib=None):
     """O, LSE of softmax(scale*Q K^T + mask) (dropout) V for [B,H,N,d] inputs."""
     L = _lib or lib()
     Q, K, V = _f64(Q), _f64(K), _f64(V)
@@ -157,7 +160,7 @@ def attn_fwd(Q, K, V, scale=None, causal=False, key_lens=None, dropout_p=0.0, se
     LSE = np.zeros((B, H, N), dtype=np.float64)
     r = L.oracle_heads_fwd(_ptr(Q, _dp), _ptr(K, _dp), _ptr(V, _dp), _ptr(O, _dp),
                            _ptr(LSE, _dp), nh, _ptr(b_idx, _ip), _ptr(h_idx, _ip),
-                           _ptr(klh, _ip), N, d, float(scale), int(bool(causal)),
+                           _ptr(klh, _ip), N, d, float(scale), int(bool(causal)), int(window),
                            float(dropout_p), int(seed), int(nthreads))
     if r != 0:
         raise ValueError("oracle_heads_fwd rejected its arguments")
@@ -165,7 +168,7 @@ def attn_fwd(Q, K, V, scale=None, causal=False, key_lens=None, dropout_p=0.0, se
 
 
 def attn_bwd(Q, K, V, dO, scale=None, causal=False, key_lens=None, dropout_p=0.0, seed=0,
-             nthreads=0, _lib=None):
+             nthreads=0, window=0, _lib=None):
     """dQ, dK, dV (and D = rowsum(dO*O)) of the same chain."""
     L = _lib or lib()
     Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
@@ -182,7 +185,7 @@ def attn_bwd(Q, K, V, dO, scale=None, causal=False, key_lens=None, dropout_p=0.0
     r = L.oracle_heads_bwd(_ptr(Q, _dp), _ptr(K, _dp), _ptr(V, _dp), _ptr(dO, _dp),
                            _ptr(dQ, _dp), _ptr(dK, _dp), _ptr(dV, _dp), _ptr(D, _dp),
                            nh, _ptr(b_idx, _ip), _ptr(h_idx, _ip), _ptr(klh, _ip),
-                           N, d, float(scale), int(bool(causal)), float(dropout_p),
+                           N, d, float(scale), int(bool(causal)), int(window), float(dropout_p),
                            int(seed), int(nthreads))
     if r != 0:
         raise ValueError("oracle_heads_bwd rejected its arguments")
@@ -190,7 +193,7 @@ def attn_bwd(Q, K, V, dO, scale=None, causal=False, key_lens=None, dropout_p=0.0
 
 
 def heads_fwd(Qh, Kh, Vh, b_idx, h_idx, key_len, scale, causal=False, dropout_p=0.0,
-              seed=0, nthreads=0, _lib=None):
+              seed=0, nthreads=0, window=0, _lib=None):
     """Forward of selected heads.  Qh..Vh: [nh, N, d]; b_idx/h_idx/key_len: [nh]."""
     L = _lib or lib()
     Qh, Kh, Vh = _f64(Qh), _f64(Kh), _f64(Vh)
@@ -202,7 +205,7 @@ def heads_fwd(Qh, Kh, Vh, b_idx, h_idx, key_len, scale, causal=False, dropout_p=
     LSE = np.zeros((nh, N), dtype=np.float64)
     r = L.oracle_heads_fwd(_ptr(Qh, _dp), _ptr(Kh, _dp), _ptr(Vh, _dp), _ptr(O, _dp),
                            _ptr(LSE, _dp), nh, _ptr(b_idx, _ip), _ptr(h_idx, _ip),
-                           _ptr(key_len, _ip), N, d, float(scale), int(bool(causal)),
+                           _ptr(key_len, _ip), N, d, float(scale), int(bool(causal)), int(window),
                            float(dropout_p), int(seed), int(nthreads))
     if r != 0:
         raise ValueError("oracle_heads_fwd rejected its arguments")
@@ -210,7 +213,7 @@ def heads_fwd(Qh, Kh, Vh, b_idx, h_idx, key_len, scale, causal=False, dropout_p=
 
 
 def heads_bwd(Qh, Kh, Vh, dOh, b_idx, h_idx, key_len, scale, causal=False, dropout_p=0.0,
-              seed=0, nthreads=0, _lib=None):
+              seed=0, nthreads=0, window=0, _lib=None):
     """Backward of selected heads.  Arrays [nh, N, d]; returns dQ, dK, dV, D."""
     L = _lib or lib()
     Qh, Kh, Vh, dOh = _f64(Qh), _f64(Kh), _f64(Vh), _f64(dOh)
@@ -223,7 +226,7 @@ def heads_bwd(Qh, Kh, Vh, dOh, b_idx, h_idx, key_len, scale, causal=False, dropo
     r = L.oracle_heads_bwd(_ptr(Qh, _dp), _ptr(Kh, _dp), _ptr(Vh, _dp), _ptr(dOh, _dp),
                            _ptr(dQ, _dp), _ptr(dK, _dp), _ptr(dV, _dp), _ptr(D, _dp),
                            nh, _ptr(b_idx, _ip), _ptr(h_idx, _ip), _ptr(key_len, _ip),
-                           N, d, float(scale), int(bool(causal)), float(dropout_p),
+                           N, d, float(scale), int(bool(causal)), int(window), float(dropout_p),
                            int(seed), int(nthreads))
     if r != 0:
         raise ValueError("oracle_heads_bwd rejected its arguments")
@@ -231,7 +234,7 @@ def heads_bwd(Qh, Kh, Vh, dOh, b_idx, h_idx, key_len, scale, causal=False, dropo
 
 
 def head_fwd_rows(q, k, v, rows, scale, causal=False, key_len=None, dropout_p=0.0, seed=0,
-                  b=0, h=0, _lib=None):
+                  b=0, h=0, window=0, _lib=None):
     """Selected rows of one head ([N, d] inputs) without an N x N array."""
     L = _lib or lib()
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -242,7 +245,7 @@ def head_fwd_rows(q, k, v, rows, scale, causal=False, key_len=None, dropout_p=0.
     LSE = np.zeros(len(rows), dtype=np.float64)
     r = L.oracle_head_fwd_rows(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(rows, _ip),
                                len(rows), _ptr(O, _dp), _ptr(LSE, _dp), N, d, float(scale),
-                               int(bool(causal)), kl, float(dropout_p), int(seed), int(b),
+                               int(bool(causal)), int(window), kl, float(dropout_p), int(seed), int(b),
                                int(h))
     if r != 0:
         raise ValueError("oracle_head_fwd_rows rejected its arguments")
@@ -250,7 +253,7 @@ def head_fwd_rows(q, k, v, rows, scale, causal=False, key_len=None, dropout_p=0.
 
 
 def head_fwd_tiled(q, k, v, scale, Br, Bc, causal=False, key_len=None, dropout_p=0.0,
-                   seed=0, b=0, h=0, _lib=None):
+                   seed=0, b=0, h=0, window=0, _lib=None):
     """One head through the online-softmax recurrence with tiles Br x Bc."""
     L = _lib or lib()
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -259,7 +262,7 @@ def head_fwd_tiled(q, k, v, scale, Br, Bc, causal=False, key_len=None, dropout_p
     O = np.zeros((N, d), dtype=np.float64)
     LSE = np.zeros(N, dtype=np.float64)
     r = L.oracle_head_fwd_tiled(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(O, _dp),
-                                _ptr(LSE, _dp), N, d, float(scale), int(bool(causal)), kl,
+                                _ptr(LSE, _dp), N, d, float(scale), int(bool(causal)), int(window), kl,
                                 float(dropout_p), int(seed), int(b), int(h), int(Br), int(Bc))
     if r != 0:
         raise ValueError("oracle_head_fwd_tiled rejected its arguments")
@@ -267,7 +270,7 @@ def head_fwd_tiled(q, k, v, scale, Br, Bc, causal=False, key_len=None, dropout_p
 
 
 def heads_rows_fwd_bwd(Qh, Kh, Vh, dOh, b_idx, h_idx, key_len, scale, row0, nrows,
-                       causal=False, dropout_p=0.0, seed=0, nthreads=0, _lib=None):
+                       causal=False, dropout_p=0.0, seed=0, nthreads=0, window=0, _lib=None):
     """Forward and backward of query rows [row0, row0+nrows) of selected heads.
 
     Returns O_rows, LSE_rows, dQ_rows ([nh, nrows, ...]) and the rows'
@@ -285,7 +288,7 @@ def heads_rows_fwd_bwd(Qh, Kh, Vh, dOh, b_idx, h_idx, key_len, scale, row0, nrow
     dV = np.zeros((nh, N, d))
     r = L.oracle_heads_rows_fwd_bwd(_ptr(Qh, _dp), _ptr(Kh, _dp), _ptr(Vh, _dp), _ptr(dOh, _dp),
                                     nh, _ptr(b_idx, _ip), _ptr(h_idx, _ip), _ptr(key_len, _ip),
-                                    N, d, float(scale), int(bool(causal)), float(dropout_p),
+                                    N, d, float(scale), int(bool(causal)), int(window), float(dropout_p),
                                     int(seed), int(row0), int(nrows), _ptr(O, _dp),
                                     _ptr(LSE, _dp), _ptr(dQ, _dp), _ptr(dK, _dp), _ptr(dV, _dp),
                                     int(nthreads))

@@ -37,7 +37,10 @@
  *
  * Readings of points the pages leave open (each also listed in the design doc):
  *   - mask: key j of sequence b is valid iff j < key_len[b] and, when causal,
- *     j <= i.  Invalid scores are -inf before the softmax.
+ *     j <= i, and, when window w > 0 (sliding-window attention, named as a
+ *     variant in "Why FlashAttention Is a Kernel Story", "When it falls down"),
+ *     i - j < w (and j - i < w when not causal).  Invalid scores are -inf
+ *     before the softmax.
  *   - a row with no valid key has O = 0, LSE = -inf and zero gradients.
  *   - dropout is inverted dropout on the normalised P: kept entries are
  *     scaled by 1/(1-p); the log-sum-exp and the softmax denominator use the
@@ -119,9 +122,13 @@ void oracle_dropout_mask(uint64_t seed, int b, int h, int rows, int cols, double
 /* ------------------------------------------------------------------------ */
 /* Shared pieces of the materialised chain                                   */
 /* ------------------------------------------------------------------------ */
-static int valid_pair(int i, int j, int causal, int key_len) {
+static int valid_pair(int i, int j, int causal, int window, int key_len) {
     if (j >= key_len) return 0;
     if (causal && j > i) return 0;
+    if (window > 0) {   /* local attention: keys within window - 1 of the query */
+        if (i - j >= window) return 0;
+        if (!causal && j - i >= window) return 0;
+    }
     return 1;
 }
 
@@ -135,13 +142,13 @@ static int check_args(int N, int d, double p, int key_len) {
 /* S (scaled, masked to -inf), then P = softmax(S) row-wise, LSE per row.
  * Rows with no valid key get P = 0 and LSE = -inf. */
 static void scores_and_probs(const double* q, const double* k, int N, int d, double scale,
-                             int causal, int key_len, double* P, double* lse) {
+                             int causal, int window, int key_len, double* P, double* lse) {
     for (int i = 0; i < N; ++i) {
         double* Pi = P + (size_t)i * N;
         double m = -INFINITY;
         for (int j = 0; j < N; ++j) {
             double s = -INFINITY;
-            if (valid_pair(i, j, causal, key_len)) {
+            if (valid_pair(i, j, causal, window, key_len)) {
                 double acc = 0.0;
                 for (int c = 0; c < d; ++c) acc += q[(size_t)i * d + c] * k[(size_t)j * d + c];
                 s = scale * acc;
@@ -182,13 +189,13 @@ static void dropout_factors(int N, double p, uint64_t seed, int b, int h, double
 /* One head, materialised                                                    */
 /* ------------------------------------------------------------------------ */
 int oracle_head_fwd(const double* q, const double* k, const double* v, double* o, double* lse,
-                    int N, int d, double scale, int causal, int key_len, double p,
+                    int N, int d, double scale, int causal, int window, int key_len, double p,
                     uint64_t seed, int b, int h) {
     if (check_args(N, d, p, key_len)) return -1;
     double* P = (double*)malloc(sizeof(double) * (size_t)N * N);
     double* F = (double*)malloc(sizeof(double) * (size_t)N * N);
     if (!P || !F) { free(P); free(F); return -2; }
-    scores_and_probs(q, k, N, d, scale, causal, key_len, P, lse);
+    scores_and_probs(q, k, N, d, scale, causal, window, key_len, P, lse);
     dropout_factors(N, p, seed, b, h, F);
     /* O_i = sum_j P_ij F_ij V_j, accumulated key by key (row-major access). */
     for (size_t x = 0; x < (size_t)N * d; ++x) o[x] = 0.0;
@@ -215,7 +222,7 @@ int oracle_head_fwd(const double* q, const double* k, const double* v, double* o
  */
 int oracle_head_bwd(const double* q, const double* k, const double* v, const double* dout,
                     double* dq, double* dk, double* dv, double* D_out,
-                    int N, int d, double scale, int causal, int key_len, double p,
+                    int N, int d, double scale, int causal, int window, int key_len, double p,
                     uint64_t seed, int b, int h) {
     if (check_args(N, d, p, key_len)) return -1;
     double* P = (double*)malloc(sizeof(double) * (size_t)N * N);
@@ -223,7 +230,7 @@ int oracle_head_bwd(const double* q, const double* k, const double* v, const dou
     double* dS = (double*)malloc(sizeof(double) * (size_t)N * N);
     double* lse = (double*)malloc(sizeof(double) * (size_t)N);
     if (!P || !F || !dS || !lse) { free(P); free(F); free(dS); free(lse); return -2; }
-    scores_and_probs(q, k, N, d, scale, causal, key_len, P, lse);
+    scores_and_probs(q, k, N, d, scale, causal, window, key_len, P, lse);
     dropout_factors(N, p, seed, b, h, F);
 
     /* dV_j = sum_i P_ij F_ij dO_i, accumulated query by query */
@@ -277,7 +284,7 @@ int oracle_head_bwd(const double* q, const double* k, const double* v, const dou
  */
 int oracle_head_fwd_rows(const double* q, const double* k, const double* v,
                          const int32_t* rows, int nrows, double* o_rows, double* lse_rows,
-                         int N, int d, double scale, int causal, int key_len, double p,
+                         int N, int d, double scale, int causal, int window, int key_len, double p,
                          uint64_t seed, int b, int h) {
     if (check_args(N, d, p, key_len)) return -1;
     double* s = (double*)malloc(sizeof(double) * (size_t)N);
@@ -290,7 +297,7 @@ int oracle_head_fwd_rows(const double* q, const double* k, const double* v,
         double m = -INFINITY;
         for (int j = 0; j < N; ++j) {
             double sc = -INFINITY;
-            if (valid_pair(i, j, causal, key_len)) {
+            if (valid_pair(i, j, causal, window, key_len)) {
                 double acc = 0.0;
                 for (int c = 0; c < d; ++c) acc += q[(size_t)i * d + c] * k[(size_t)j * d + c];
                 sc = scale * acc;
@@ -331,7 +338,7 @@ int oracle_head_fwd_rows(const double* q, const double* k, const double* v,
 int oracle_head_rows_fwd_bwd(const double* q, const double* k, const double* v,
                              const double* dout, int row0, int nrows, double* o_rows,
                              double* lse_rows, double* dq_rows, double* dk_part, double* dv_part,
-                             int N, int d, double scale, int causal, int key_len, double p,
+                             int N, int d, double scale, int causal, int window, int key_len, double p,
                              uint64_t seed, int b, int h) {
     if (check_args(N, d, p, key_len) || row0 < 0 || nrows < 0 || row0 + nrows > N) return -1;
     double* P = (double*)malloc(sizeof(double) * (size_t)N);
@@ -349,7 +356,7 @@ int oracle_head_rows_fwd_bwd(const double* q, const double* k, const double* v,
         double m = -INFINITY;
         for (int j = 0; j < N; ++j) {
             double sc = -INFINITY;
-            if (valid_pair(i, j, causal, key_len)) {
+            if (valid_pair(i, j, causal, window, key_len)) {
                 double acc = 0.0;
                 for (int c = 0; c < d; ++c) acc += qi[c] * k[(size_t)j * d + c];
                 sc = scale * acc;
@@ -401,7 +408,7 @@ int oracle_head_rows_fwd_bwd(const double* q, const double* k, const double* v,
 int oracle_heads_rows_fwd_bwd(const double* Q, const double* K, const double* V,
                               const double* dO, int nh, const int32_t* b_idx,
                               const int32_t* h_idx, const int32_t* key_len, int N, int d,
-                              double scale, int causal, double p, uint64_t seed, int row0,
+                              double scale, int causal, int window, double p, uint64_t seed, int row0,
                               int nrows, double* O_rows, double* LSE_rows, double* dQ_rows,
                               double* dK_part, double* dV_part, int nthreads);
 
@@ -417,7 +424,7 @@ int oracle_heads_rows_fwd_bwd(const double* Q, const double* K, const double* V,
  * terms that enter O (not l) by Z/(1-p).
  */
 int oracle_head_fwd_tiled(const double* q, const double* k, const double* v, double* o,
-                          double* lse, int N, int d, double scale, int causal, int key_len,
+                          double* lse, int N, int d, double scale, int causal, int window, int key_len,
                           double p, uint64_t seed, int b, int h, int Br, int Bc) {
     if (check_args(N, d, p, key_len) || Br < 1 || Bc < 1) return -1;
     double* m = (double*)malloc(sizeof(double) * (size_t)Br);
@@ -439,7 +446,7 @@ int oracle_head_fwd_tiled(const double* q, const double* k, const double* v, dou
                 for (int cc = 0; cc < bc; ++cc) {
                     int j = j0 + cc;
                     double sc = -INFINITY;
-                    if (valid_pair(i, j, causal, key_len)) {
+                    if (valid_pair(i, j, causal, window, key_len)) {
                         double a = 0.0;
                         for (int c = 0; c < d; ++c) a += q[(size_t)i * d + c] * k[(size_t)j * d + c];
                         sc = scale * a;
@@ -498,7 +505,7 @@ static void set_threads(int nthreads) {
 
 int oracle_heads_fwd(const double* Q, const double* K, const double* V, double* O, double* LSE,
                      int nh, const int32_t* b_idx, const int32_t* h_idx, const int32_t* key_len,
-                     int N, int d, double scale, int causal, double p, uint64_t seed,
+                     int N, int d, double scale, int causal, int window, double p, uint64_t seed,
                      int nthreads) {
     if (nh < 0) return -1;
     set_threads(nthreads);
@@ -507,7 +514,7 @@ int oracle_heads_fwd(const double* Q, const double* K, const double* V, double* 
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
     for (int x = 0; x < nh; ++x) {
         int r = oracle_head_fwd(Q + x * hd, K + x * hd, V + x * hd, O + x * hd, LSE + (size_t)x * N,
-                                N, d, scale, causal, key_len[x], p, seed, b_idx[x], h_idx[x]);
+                                N, d, scale, causal, window, key_len[x], p, seed, b_idx[x], h_idx[x]);
         if (r) err |= 1;
     }
     return err ? -1 : 0;
@@ -516,7 +523,7 @@ int oracle_heads_fwd(const double* Q, const double* K, const double* V, double* 
 int oracle_heads_bwd(const double* Q, const double* K, const double* V, const double* dO,
                      double* dQ, double* dK, double* dV, double* D,
                      int nh, const int32_t* b_idx, const int32_t* h_idx, const int32_t* key_len,
-                     int N, int d, double scale, int causal, double p, uint64_t seed,
+                     int N, int d, double scale, int causal, int window, double p, uint64_t seed,
                      int nthreads) {
     if (nh < 0) return -1;
     set_threads(nthreads);
@@ -527,7 +534,7 @@ int oracle_heads_bwd(const double* Q, const double* K, const double* V, const do
         int r = oracle_head_bwd(Q + x * hd, K + x * hd, V + x * hd, dO + x * hd,
                                 dQ + x * hd, dK + x * hd, dV + x * hd,
                                 D ? D + (size_t)x * N : NULL,
-                                N, d, scale, causal, key_len[x], p, seed, b_idx[x], h_idx[x]);
+                                N, d, scale, causal, window, key_len[x], p, seed, b_idx[x], h_idx[x]);
         if (r) err |= 1;
     }
     return err ? -1 : 0;
@@ -536,7 +543,7 @@ int oracle_heads_bwd(const double* Q, const double* K, const double* V, const do
 int oracle_heads_rows_fwd_bwd(const double* Q, const double* K, const double* V,
                               const double* dO, int nh, const int32_t* b_idx,
                               const int32_t* h_idx, const int32_t* key_len, int N, int d,
-                              double scale, int causal, double p, uint64_t seed, int row0,
+                              double scale, int causal, int window, double p, uint64_t seed, int row0,
                               int nrows, double* O_rows, double* LSE_rows, double* dQ_rows,
                               double* dK_part, double* dV_part, int nthreads) {
     if (nh < 0) return -1;
@@ -549,7 +556,7 @@ int oracle_heads_rows_fwd_bwd(const double* Q, const double* K, const double* V,
         int r = oracle_head_rows_fwd_bwd(Q + x * hd, K + x * hd, V + x * hd, dO + x * hd, row0,
                                          nrows, O_rows + x * rd, LSE_rows + (size_t)x * nrows,
                                          dQ_rows + x * rd, dK_part + x * hd, dV_part + x * hd, N, d,
-                                         scale, causal, key_len[x], p, seed, b_idx[x], h_idx[x]);
+                                         scale, causal, window, key_len[x], p, seed, b_idx[x], h_idx[x]);
         if (r) err |= 1;
     }
     return err ? -1 : 0;

@@ -30,12 +30,16 @@ def _rand(*shape, scale=1.0, seed=None):
     return r.standard_normal(shape) * scale
 
 
-def _valid(N, causal, key_len):
+def _valid(N, causal, key_len, window=0):
     i = np.arange(N)[:, None]
     j = np.arange(N)[None, :]
     v = np.broadcast_to(j < key_len, (N, N))
     if causal:
         v = v & (j <= i)
+    if window > 0:   # sliding window: keys within window - 1 of the query
+        v = v & (i - j < window)
+        if not causal:
+            v = v & (j - i < window)
     return np.array(v)
 
 
@@ -150,11 +154,11 @@ def pin_key_shift_invariance(L) -> float:
 # ---------------------------------------------------------------------------
 # library routines computing the same chain another way
 # ---------------------------------------------------------------------------
-def _torch_chain(q, k, v, scale, causal, key_len, p, Z):
+def _torch_chain(q, k, v, scale, causal, key_len, p, Z, window=0):
     """softmax(scale Q K^T + mask) * Z/(1-p) @ V with torch float64 library ops."""
     s = scale * torch.matmul(q, k.transpose(-1, -2))
     N = q.shape[-2]
-    valid = torch.as_tensor(_valid(N, causal, key_len))
+    valid = torch.as_tensor(_valid(N, causal, key_len, window))
     s = s.masked_fill(~valid, float("-inf"))
     lse = torch.logsumexp(s, dim=-1)
     P = torch.softmax(s, dim=-1)
@@ -184,6 +188,47 @@ def pin_torch_autograd(L) -> float:
             worst = max(worst, np.abs(LSE[0, h] - tl.detach().numpy()).max())
             for g, tg in ((dQ, tq), (dK, tk), (dV, tv)):
                 worst = max(worst, np.abs(g[0, h] - tg.grad.numpy()).max())
+    return worst
+
+
+def pin_window_one(L) -> float:
+    """Sliding window of width 1: each query sees only its own key, so O_i = V_i
+    and LSE_i = scale q_i . k_i, causal or not."""
+    worst = 0.0
+    for causal in (False, True):
+        N, d = 9, 6
+        q, k, v = (_rand(1, 1, N, d, seed=s) for s in (21, 22, 23))
+        O, LSE = oracle.attn_fwd(q, k, v, 0.8, causal, None, 0.0, 0, window=1, _lib=L)
+        worst = max(worst, np.abs(O - v).max())
+        worst = max(worst, np.abs(LSE[0, 0] - 0.8 * np.einsum("nd,nd->n", q[0, 0], k[0, 0])).max())
+    return worst
+
+
+def pin_window_torch(L) -> float:
+    """Sliding-window masks (causal and two-sided) against torch float64 for the
+    forward and torch autograd for the backward, with key padding and dropout;
+    a window of at least N gives exactly the unwindowed result."""
+    worst = 0.0
+    for N, d, causal, key_len, p, w in ((13, 4, True, 13, 0.0, 3), (16, 8, False, 12, 0.0, 4),
+                                        (19, 4, True, 15, 0.3, 5), (11, 8, False, 11, 0.2, 2)):
+        B, H = 1, 2
+        q, k, v, do = (_rand(B, H, N, d) for _ in range(4))
+        sc = 1 / math.sqrt(d)
+        O, LSE = oracle.attn_fwd(q, k, v, sc, causal, [key_len], p, 7, window=w, _lib=L)
+        dQ, dK, dV, _ = oracle.attn_bwd(q, k, v, do, sc, causal, [key_len], p, 7, window=w, _lib=L)
+        for h in range(H):
+            Z = oracle.dropout_mask(7, 0, h, N, N, p, _lib=L) if p > 0 else None
+            tq, tk, tv = (torch.tensor(a[0, h], requires_grad=True) for a in (q, k, v))
+            to, tl = _torch_chain(tq, tk, tv, sc, causal, key_len, p, Z, window=w)
+            (to * torch.tensor(do[0, h])).sum().backward()
+            worst = max(worst, np.abs(O[0, h] - to.detach().numpy()).max())
+            fin = np.isfinite(LSE[0, h])
+            worst = max(worst, np.abs(LSE[0, h][fin] - tl.detach().numpy()[fin]).max())
+            for g, tg in ((dQ, tq), (dK, tk), (dV, tv)):
+                worst = max(worst, np.abs(g[0, h] - tg.grad.numpy()).max())
+        O2, LSE2 = oracle.attn_fwd(q, k, v, sc, causal, [key_len], p, 7, window=N, _lib=L)
+        O3, LSE3 = oracle.attn_fwd(q, k, v, sc, causal, [key_len], p, 7, _lib=L)
+        worst = max(worst, np.abs(O2 - O3).max(), np.abs(np.nan_to_num(LSE2 - LSE3)).max())
     return worst
 
 
@@ -381,6 +426,8 @@ PINS = {
     "two_keys_sigmoid": (pin_two_keys_sigmoid, 1e-13),
     "key_shift_invariance": (pin_key_shift_invariance, 1e-12),
     "torch_autograd": (pin_torch_autograd, 1e-12),
+    "window_one": (pin_window_one, 1e-12),
+    "window_torch": (pin_window_torch, 1e-12),
     "finite_differences": (pin_finite_differences, 1e-6),
     "dk_sums_to_zero": (pin_dk_sums_to_zero, 1e-12),
     "D_equals_dO_dot_O": (pin_D_equals_dO_dot_O, 1e-12),

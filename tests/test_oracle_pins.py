@@ -56,6 +56,8 @@ MUTATIONS = {
     "dV_transposed": ("dv[(size_t)j * d + c] += w * dout[(size_t)i * d + c];",
                       "dv[(size_t)i * d + c] += w * dout[(size_t)j * d + c];"),
     "causal_off_by_one": ("if (causal && j > i) return 0;", "if (causal && j >= i) return 0;"),
+    "window_off_by_one": ("if (i - j >= window) return 0;", "if (i - j > window) return 0;"),
+    "window_one_sided": ("if (!causal && j - i >= window) return 0;", "if (0) return 0;"),
     "scores_unscaled": ("                s = scale * acc;\n", "                s = acc;\n"),
     "dropout_no_rescale": ("oracle_dropout_keep(seed, b, h, i, j, t) ? inv : 0.0;",
                            "oracle_dropout_keep(seed, b, h, i, j, t) ? 1.0 : 0.0;"),
