@@ -24,6 +24,8 @@ import statistics
 import subprocess
 import sys
 import tempfile
+
+import numpy as np
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -41,6 +43,17 @@ L2_BYTES = 129 * 2**20
 # ---------------------------------------------------------------------------
 # algorithmic work
 # ---------------------------------------------------------------------------
+def window_flops_fwd(w: Workload, window: int) -> float:
+    """4 d FLOPs per attended (query, key) pair under a sliding window of
+    `window` keys (causal: i - window < j <= i; else |i - j| < window)."""
+    i = np.arange(w.N)
+    if w.causal:
+        pairs = np.minimum(i + 1, window).sum()
+    else:
+        pairs = (np.minimum(i + window, w.N) - np.maximum(0, i - window + 1)).sum()
+    return 4.0 * w.B * w.H * w.d * float(pairs)
+
+
 def fwd_compulsory_bytes(w: Workload) -> int:
     """Q, K, V read and O written once, plus one fp32 LSE per row."""
     es = 2 if w.dtype == "bf16" else 4
@@ -281,7 +294,7 @@ def run_ours(args, w: Workload):
         dq, dk, dv = (torch.empty_like(q) for _ in range(3))
         ws = torch.empty(ea.attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    kw = dict(causal=w.causal, key_lens=kl, dropout_p=inp.dropout_p, seed=inp.seed,
+    kw = dict(causal=w.causal, window=args.window, key_lens=kl, dropout_p=inp.dropout_p, seed=inp.seed,
               scale=inp.scale)
 
     def step(evs=None):
@@ -346,7 +359,8 @@ def run_ours(args, w: Workload):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
 
-    flops_fwd, flops_bwd = w.flops_fwd(), (w.flops_bwd() if bwd else 0.0)
+    flops_fwd = w.flops_fwd() if args.window <= 0 else window_flops_fwd(w, args.window)
+    flops_bwd = (2.5 * flops_fwd) if bwd else 0.0
     flops_step = flops_fwd + flops_bwd
     value = world * flops_step * args.steps / (elapsed_ms * 1e-3) / 1e12
     fwd_ms, pre_ms, main_ms, conv_ms = (statistics.mean(x) for x in per)
@@ -406,7 +420,8 @@ def run_ours(args, w: Workload):
                "ms_per_step": e_ms / args.e2e_steps}
 
     cpu = None
-    if world == 1 and not args.no_cpu_baseline and bwd:   # the sample is forward+backward
+    # the sample is forward+backward of the default (unwindowed) configuration
+    if world == 1 and not args.no_cpu_baseline and bwd and args.window <= 0:
         cpu = cpu_baseline(inp, w, target_s=args.cpu_seconds)
 
     l2_note = (f"inputs {in_bytes / 2**20:.0f} MiB <= L2: L2 flushed (256 MiB write) before every step"
@@ -420,6 +435,7 @@ def run_ours(args, w: Workload):
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                    "causal": w.causal, "dropout_p": w.dropout_p,
                    "passes": "fwd+bwd" if bwd else "fwd",
+                   "window": args.window if args.window > 0 else None,
                    "global_batch": world * w.B, "seq_len": w.N,
                    "parallelism": f"replicas x{world} (heads independent)",
                    "l2": l2_note},
@@ -443,6 +459,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, help="1-based workload index")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding window of this many keys (FLOPs count the attended pairs exactly)")
     ap.add_argument("--dtype", choices=["default", "fp16"], default="default",
                     help="fp16: store the workload's inputs as IEEE half (16-bit workloads only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -69,16 +69,16 @@ def library():
             lib = ctypes.CDLL(LIB_PATH)
             vp, ip, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
             f, u64 = ctypes.c_float, ctypes.c_uint64
-            lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, f, ip, vp, f, u64,
+            lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, f, ip, ip, vp, f, u64,
                                      vp, vp]
-            lib.attn_bwd.argtypes = [vp] * 9 + [ip, ip, ip, ip, ip, f, ip, vp, f, u64, vp, sz,
+            lib.attn_bwd.argtypes = [vp] * 9 + [ip, ip, ip, ip, ip, f, ip, ip, vp, f, u64, vp, sz,
                                                 vp, vp]
-            lib.attn_bwd_noalloc.argtypes = [vp] * 9 + [ip, ip, ip, ip, ip, f, ip, vp, f, u64,
+            lib.attn_bwd_noalloc.argtypes = [vp] * 9 + [ip, ip, ip, ip, ip, f, ip, ip, vp, f, u64,
                                                         vp, vp]
             lib.attn_bwd_workspace_size.argtypes = [ip, ip, ip, ip]
             lib.attn_bwd_workspace_size.restype = sz
             lib.attn_bwd_preprocess.argtypes = [vp, vp, vp, ip, ip, ip, ip, ip, vp, sz, vp]
-            lib.attn_bwd_main.argtypes = [vp] * 6 + [ip, ip, ip, ip, ip, f, ip, vp, f, u64, vp,
+            lib.attn_bwd_main.argtypes = [vp] * 6 + [ip, ip, ip, ip, ip, f, ip, ip, vp, f, u64, vp,
                                                      sz, vp, vp]
             lib.attn_bwd_dq_convert.argtypes = [vp, ip, ip, ip, ip, ip, f, vp, sz, vp]
             for fn in ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
@@ -155,7 +155,8 @@ def _raise(st: int, where: str):
 # ---------------------------------------------------------------------------
 # entry points
 # ---------------------------------------------------------------------------
-def attn_fwd(q, k, v, *, causal: bool = False, key_lens=None, dropout_p: float = 0.0,
+def attn_fwd(q, k, v, *, causal: bool = False, window: int = 0, key_lens=None,
+             dropout_p: float = 0.0,
              seed: int = 0, scale: Optional[float] = None, out=None, lse=None,
              dev_status=None, stream=None):
     """O, LSE = attention(q, k, v); see include/gbattn.h for the exact contract."""
@@ -172,7 +173,7 @@ def attn_fwd(q, k, v, *, causal: bool = False, key_lens=None, dropout_p: float =
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     kl = _key_lens(key_lens, q)
     st = library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
-                            _dtype_code(q), float(scale), int(bool(causal)), _ptr(kl),
+                            _dtype_code(q), float(scale), int(bool(causal)), int(window), _ptr(kl),
                             float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(dev_status),
                             _stream(stream))
     _raise(st, "attn_fwd")
@@ -186,7 +187,7 @@ def _workspace(B, H, N, d, workspace, device):
     return workspace, int(workspace.numel() * workspace.element_size())
 
 
-def attn_bwd(q, k, v, o, do, lse, *, causal: bool = False, key_lens=None,
+def attn_bwd(q, k, v, o, do, lse, *, causal: bool = False, window: int = 0, key_lens=None,
              dropout_p: float = 0.0, seed: int = 0, scale: Optional[float] = None, dq=None,
              dk=None, dv=None, workspace=None, dev_status=None, stream=None):
     """dQ, dK, dV of attention given the forward's o and lse and the gradient do."""
@@ -204,14 +205,15 @@ def attn_bwd(q, k, v, o, do, lse, *, causal: bool = False, key_lens=None,
     kl = _key_lens(key_lens, q)
     st = library().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
                             _ptr(dk), _ptr(dv), B, H, N, d, _dtype_code(q), float(scale),
-                            int(bool(causal)), _ptr(kl), float(dropout_p),
+                            int(bool(causal)), int(window), _ptr(kl), float(dropout_p),
                             int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(ws), ws_bytes, _ptr(dev_status),
                             _stream(stream))
     _raise(st, "attn_bwd")
     return dq, dk, dv
 
 
-def attn_bwd_noalloc(q, k, v, o, do, lse, *, causal: bool = False, key_lens=None,
+def attn_bwd_noalloc(q, k, v, o, do, lse, *, causal: bool = False, window: int = 0,
+                     key_lens=None,
                      dropout_p: float = 0.0, seed: int = 0, scale: Optional[float] = None,
                      dq=None, dk=None, dv=None, dev_status=None, stream=None):
     """attn_bwd using the library's built-in 32 MiB scratch instead of a
@@ -230,7 +232,7 @@ def attn_bwd_noalloc(q, k, v, o, do, lse, *, causal: bool = False, key_lens=None
     kl = _key_lens(key_lens, q)
     st = library().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
                                     _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, _dtype_code(q),
-                                    float(scale), int(bool(causal)), _ptr(kl), float(dropout_p),
+                                    float(scale), int(bool(causal)), int(window), _ptr(kl), float(dropout_p),
                                     int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(dev_status),
                                     _stream(stream))
     _raise(st, "attn_bwd_noalloc")
@@ -247,14 +249,14 @@ def attn_bwd_preprocess(o, do, lse, workspace, *, stream=None):
     _raise(st, "attn_bwd_preprocess")
 
 
-def attn_bwd_main(q, k, v, do, dk, dv, workspace, *, causal=False, key_lens=None,
+def attn_bwd_main(q, k, v, do, dk, dv, workspace, *, causal=False, window=0, key_lens=None,
                   dropout_p=0.0, seed=0, scale=None, dev_status=None, stream=None):
     B, H, N, d = _shape(q)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     kl = _key_lens(key_lens, q)
     st = library().attn_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dk), _ptr(dv), B, H,
-                                 N, d, _dtype_code(q), float(scale), int(bool(causal)), _ptr(kl),
+                                 N, d, _dtype_code(q), float(scale), int(bool(causal)), int(window), _ptr(kl),
                                  float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF,
                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _ptr(dev_status), _stream(stream))

@@ -110,7 +110,7 @@ using namespace gbattn;
 extern "C" {
 
 attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
-                     int H, int N, int d, attn_dtype dtype, float scale, int causal,
+                     int H, int N, int d, attn_dtype dtype, float scale, int causal, int window,
                      const int32_t* key_lens, float dropout_p, uint64_t seed, int* dev_status,
                      void* stream) {
     if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
@@ -138,6 +138,7 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
     p.drop_threshold = drop_threshold(dropout_p);
     p.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFu);
     p.seed_hi = static_cast<uint32_t>(seed >> 32);
+    p.window = window > 0 ? window : 0;
     return from_cuda(launch_fwd(tq, tk, tv, p, d, dtype, causal != 0, dropout_p > 0.f,
                                 static_cast<cudaStream_t>(stream)));
 }
@@ -162,7 +163,8 @@ attn_status attn_bwd_preprocess(const void* O, const void* dO, const float* LSE,
 
 attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dK,
                           void* dV, int B, int H, int N, int d, attn_dtype dtype, float scale,
-                          int causal, const int32_t* key_lens, float dropout_p, uint64_t seed,
+                          int causal, int window, const int32_t* key_lens, float dropout_p,
+                          uint64_t seed,
                           void* workspace, size_t workspace_bytes, int* dev_status,
                           void* stream) {
     if (!Q || !K || !V || !dO || !dK || !dV) return ATTN_ERR_INVALID_ARG;
@@ -198,6 +200,7 @@ attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const voi
     p.drop_threshold = drop_threshold(dropout_p);
     p.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFu);
     p.seed_hi = static_cast<uint32_t>(seed >> 32);
+    p.window = window > 0 ? window : 0;
     return from_cuda(launch_bwd_main(tq, tk, tv, tdo, tdk, tdv, p, d, dtype == ATTN_DTYPE_FP16,
                                      causal != 0, dropout_p > 0.f,
                                      static_cast<cudaStream_t>(stream)));
@@ -220,7 +223,7 @@ attn_status attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, attn_dtype
 
 attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                      const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
-                     attn_dtype dtype, float scale, int causal, const int32_t* key_lens,
+                     attn_dtype dtype, float scale, int causal, int window, const int32_t* key_lens,
                      float dropout_p, uint64_t seed, void* workspace, size_t workspace_bytes,
                      int* dev_status, void* stream) {
     // Validate everything before the first launch so that errors leave the
@@ -236,7 +239,7 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
     if ((st = attn_bwd_preprocess(O, dO, LSE, B, H, N, d, dtype, workspace, workspace_bytes,
                                   stream)) != ATTN_OK)
         return st;
-    if ((st = attn_bwd_main(Q, K, V, dO, dK, dV, B, H, N, d, dtype, scale, causal, key_lens,
+    if ((st = attn_bwd_main(Q, K, V, dO, dK, dV, B, H, N, d, dtype, scale, causal, window, key_lens,
                             dropout_p, seed, workspace, workspace_bytes, dev_status, stream)) !=
         ATTN_OK)
         return st;

@@ -189,7 +189,7 @@ struct BwdCfg {
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <int D, bool kF16, bool kCausal, bool kDropout>
+template <int D, bool kF16, bool kCausal, bool kDropout, bool kWindow>
 __global__ void __launch_bounds__(448, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
@@ -234,8 +234,16 @@ __global__ void __launch_bounds__(448, 1)
             atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_CUDA));
         return;
     }
-    const int q_begin = kCausal ? kb : 0;
-    const int nq = p.nkb - q_begin;
+    // Query blocks that see some key of this block: from the diagonal on when
+    // causal; a sliding window of W keys also bounds them from the other side.
+    const int W = kWindow ? p.window : 0;   // compile-time 0 without a window
+    int q_begin = kCausal ? kb : 0;
+    int q_end = p.nkb;
+    if (W > 0) {
+        q_end = min(p.nkb, (k0 + kTileRows - 1 + W - 1) / kTileRows + 1);
+        if (!kCausal) q_begin = max(0, k0 - W + 1) / kTileRows;
+    }
+    const int nq = q_end - q_begin;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* bar_kv = bars + 0;
@@ -484,6 +492,9 @@ __global__ void __launch_bounds__(448, 1)
             const float* d_s = sD + stage * kTileRows + 64 * hh;
             const int q0h = qi * kTileRows + 64 * hh;   // first query of this half
             const bool diag = kCausal && (qi == kb);
+            // some (query, key) pair of this block lies outside the window
+            const bool wmask = W > 0 && (qi * kTileRows + kTileRows - 1 - k0 >= W ||
+                                         (!kCausal && k0 + kTileRows - 1 - qi * kTileRows >= W));
             // ---- phase 1 (while dP^T is still on the tensor pipe): P from S ----
             // 16-column chunks; the next chunk's TMEM load overlaps this chunk's
             // math.  P (undropped, fp32) stays in registers for phase 2.
@@ -537,7 +548,9 @@ __global__ void __launch_bounds__(448, 1)
                         const int col = 16 * c + 2 * e + u;
                         float x = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), p.scale_log2,
                                                   -lv[2 * e + u]));
-                        const bool valid = row_valid && (!diag || j <= q0h + col);
+                        const int iq = q0h + col;   // query index
+                        const bool valid = row_valid && (!diag || j <= iq) &&
+                                           (!wmask || (iq - j < W && (kCausal || j - iq < W)));
                         x = valid ? x : 0.f;
                         pr[col] = x;
                         pd[u] = x;
@@ -729,12 +742,12 @@ __global__ void __launch_bounds__(448, 1)
         atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_DEVICE_TIMEOUT));
 }
 
-template <int D, bool kF16, bool kCausal, bool kDropout>
+template <int D, bool kF16, bool kCausal, bool kDropout, bool kWindow>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                          const BwdParams& p, cudaStream_t stream) {
     using C = BwdCfg<D, kF16>;
-    auto kern = attn_bwd_kernel<D, kF16, kCausal, kDropout>;
+    auto kern = attn_bwd_kernel<D, kF16, kCausal, kDropout, kWindow>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -746,15 +759,24 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     return cudaGetLastError();
 }
 
+template <int D, bool kF16, bool kWindow>
+cudaError_t dispatch_bwd_w(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                           const BwdParams& p, bool causal, bool dropout, cudaStream_t s) {
+    if (causal)
+        return dropout ? launch_bwd_t<D, kF16, true, true, kWindow>(tq, tk, tv, tdo, tdk, tdv, p, s)
+                       : launch_bwd_t<D, kF16, true, false, kWindow>(tq, tk, tv, tdo, tdk, tdv, p, s);
+    return dropout ? launch_bwd_t<D, kF16, false, true, kWindow>(tq, tk, tv, tdo, tdk, tdv, p, s)
+                   : launch_bwd_t<D, kF16, false, false, kWindow>(tq, tk, tv, tdo, tdk, tdv, p, s);
+}
+
 template <int D, bool kF16>
 cudaError_t dispatch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                          const BwdParams& p, bool causal, bool dropout, cudaStream_t s) {
-    if (causal)
-        return dropout ? launch_bwd_t<D, kF16, true, true>(tq, tk, tv, tdo, tdk, tdv, p, s)
-                       : launch_bwd_t<D, kF16, true, false>(tq, tk, tv, tdo, tdk, tdv, p, s);
-    return dropout ? launch_bwd_t<D, kF16, false, true>(tq, tk, tv, tdo, tdk, tdv, p, s)
-                   : launch_bwd_t<D, kF16, false, false>(tq, tk, tv, tdo, tdk, tdv, p, s);
+    return p.window > 0
+               ? dispatch_bwd_w<D, kF16, true>(tq, tk, tv, tdo, tdk, tdv, p, causal, dropout, s)
+               : dispatch_bwd_w<D, kF16, false>(tq, tk, tv, tdo, tdk, tdv, p, causal, dropout, s);
 }
 
 template <int D, bool kF16>

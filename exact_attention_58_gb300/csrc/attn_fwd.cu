@@ -88,7 +88,7 @@ __device__ __forceinline__ void store_v_transposed(const float* __restrict__ Vh,
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <int D, bool kTF32, bool kF16, bool kCausal, bool kDropout>
+template <int D, bool kTF32, bool kF16, bool kCausal, bool kDropout, bool kWindow>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
@@ -129,20 +129,35 @@ __global__ void __launch_bounds__(320, 1)
     }
     const int q0 = qb * kFwdRowsPerCta;
     const int nkv_all = (L + kTileRows - 1) / kTileRows;
-    int nkv_t[2];
+    // > 0: sliding window, keys with row - key < W (and key - row < W unless
+    // causal); a compile-time 0 in the instantiations without a window
+    const int W = kWindow ? p.window : 0;
+    // Key blocks [jlo(t), jhi(t)) tile t needs (causal and window bounds skip
+    // the rest).  Scalars and selects, not arrays: a loop-indexed array would
+    // live in local memory inside the MMA issue loop.
+    int jlo0 = 0, jlo1 = 0, jhi0 = 0, jhi1 = 0;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
         const int first = q0 + t * kTileRows;
-        if (first >= N) {
-            nkv_t[t] = 0;
-        } else if (kCausal) {
+        int lo = 0, hi = 0;
+        if (first < N) {
             const int last = min(first + kTileRows - 1, N - 1);
-            nkv_t[t] = min(nkv_all, last / kTileRows + 1);
-        } else {
-            nkv_t[t] = nkv_all;
+            hi = kCausal ? min(nkv_all, last / kTileRows + 1) : nkv_all;
+            if (W > 0) {
+                lo = max(0, first - W + 1) / kTileRows;
+                if (!kCausal) hi = min(nkv_all, (last + W - 1) / kTileRows + 1);
+            }
+            lo = min(lo, hi);
         }
+        if (t == 0) { jlo0 = lo; jhi0 = hi; } else { jlo1 = lo; jhi1 = hi; }
     }
-    const int nkv = max(nkv_t[0], nkv_t[1]);
+    auto jlo = [&](int t) { return t ? jlo1 : jlo0; };
+    auto jhi = [&](int t) { return t ? jhi1 : jhi0; };
+    auto nkv_t = [&](int t) { return jhi(t) - jlo(t); };   // blocks tile t sees
+    // blocks the CTA walks: tile A's window starts no later than tile B's
+    const int jbeg = (nkv_t(0) > 0) ? jlo0 : jlo1;
+    const int jend = max(jhi0, jhi1);
+    const int nkv = (nkv_t(0) > 0 || nkv_t(1) > 0) ? jend - jbeg : 0;
 
     // ---- set-up ----
     if (threadIdx.x == 0) {
@@ -180,7 +195,7 @@ __global__ void __launch_bounds__(320, 1)
                 tma_prefetch_desc(&tmQ);
                 tma_prefetch_desc(&tmK);
                 tma_prefetch_desc(&tmV);
-                const int ntiles = (nkv_t[1] > 0) ? 2 : 1;
+                const int ntiles = (nkv_t(1) > 0) ? 2 : 1;
                 mbar_arrive_expect_tx(bar_q, ntiles * C::TILE);
                 for (int t = 0; t < ntiles; ++t)
                     for (int cb = 0; cb < C::NCB; ++cb)
@@ -189,7 +204,7 @@ __global__ void __launch_bounds__(320, 1)
             }
             int seq = 0;
             bool ok = true;
-            for (int j = 0; j < nkv && ok; ++j) {
+            for (int j = jbeg; j < jbeg + nkv && ok; ++j) {
                 for (int which = 0; which < 2; ++which) {
                     const int slot = seq % C::NSLOT;
                     const uint32_t ph = (seq / C::NSLOT) & 1;
@@ -263,7 +278,7 @@ __global__ void __launch_bounds__(320, 1)
             int v_slot = 0;
             uint32_t v_phase = 0;
             bool v_ready = false;
-            for (int j = 0; j < nkv && ok; ++j) {
+            for (int j = jbeg; j < jbeg + nkv && ok; ++j) {
                 const int kslot = seq % C::NSLOT;
                 const uint32_t kph = (seq / C::NSLOT) & 1;
                 ++seq;
@@ -272,17 +287,18 @@ __global__ void __launch_bounds__(320, 1)
                 ++seq;
                 bool k_ready = false;
                 for (int t = 0; t < 2 && ok; ++t) {
-                    const bool qk = j < nkv_t[t];
-                    const bool last_pv = (j == nkv_t[t]) && j > 0;
-                    if ((qk && j > 0) || last_pv) {   // O_t += P_t(j-1) V_{j-1}
-                        ok = mbar_wait(&bar_p[t], (j - 1) & 1, s_abort);
+                    const bool qk = j >= jlo(t) && j < jhi(t);
+                    const bool prev = j - 1 >= jlo(t) && j - 1 < jhi(t);   // tile t saw block j-1
+                    const bool last_pv = prev && j == jhi(t);
+                    if (prev) {   // O_t += P_t(j-1) V_{j-1}
+                        ok = mbar_wait(&bar_p[t], (j - 1 - jlo(t)) & 1, s_abort);
                         if (ok && !v_ready) {
                             ok = mbar_wait(&full[v_slot], v_phase, s_abort);
                             v_ready = true;
                         }
                         if (!ok) break;
                         tc_fence_after();
-                        issue_pv(t, v_slot, j - 1 > 0);
+                        issue_pv(t, v_slot, j - 1 > jlo(t));
                         if (last_pv) tc_commit(&bar_o[t]);
                     }
                     if (qk) {                         // S_t = Q_t K_j^T
@@ -298,21 +314,21 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 if (!ok) break;
                 tc_commit(&empty[kslot]);
-                if (j > 0) tc_commit(&empty[v_slot]);
+                if (j > jbeg) tc_commit(&empty[v_slot]);
                 v_slot = next_v_slot;
                 v_phase = next_v_phase;
                 v_ready = false;
             }
-            for (int t = 0; t < 2 && ok; ++t) {   // tiles whose last block is nkv-1
-                if (nkv_t[t] != nkv) continue;
-                ok = mbar_wait(&bar_p[t], (nkv - 1) & 1, s_abort);
+            for (int t = 0; t < 2 && ok; ++t) {   // tiles whose last block is the CTA's last
+                if (nkv_t(t) == 0 || jhi(t) != jbeg + nkv) continue;
+                ok = mbar_wait(&bar_p[t], (jhi(t) - 1 - jlo(t)) & 1, s_abort);
                 if (ok && !v_ready) {
                     ok = mbar_wait(&full[v_slot], v_phase, s_abort);
                     v_ready = true;
                 }
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(t, v_slot, nkv - 1 > 0);
+                issue_pv(t, v_slot, jhi(t) - 1 > jlo(t));
                 tc_commit(&bar_o[t]);
             }
             // Drain: no MMA of this CTA is in flight at teardown.
@@ -327,7 +343,7 @@ __global__ void __launch_bounds__(320, 1)
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const int row = q0 + t * kTileRows + r;
-        const int ntile = nkv_t[t];
+        const int ntile = nkv_t(t);
         const int tile_first_row = q0 + t * kTileRows;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const uint32_t t_S = t_lane + 128u * t;
@@ -335,17 +351,25 @@ __global__ void __launch_bounds__(320, 1)
         float m_ref = -INFINITY;   // reference max, log2 units of scaled scores
         float l = 0.f;
         bool ok = true;
-        for (int j = 0; j < ntile; ++j) {
-            if (!mbar_wait_warp(&bar_s[t], j & 1, s_abort)) {
+        for (int j = jlo(t); j < jhi(t); ++j) {
+            if (!mbar_wait_warp(&bar_s[t], (j - jlo(t)) & 1, s_abort)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const int k0 = j * kTileRows;
+            const int tile_last_row = tile_first_row + kTileRows - 1;
+            const bool wmask = W > 0 && (k0 < tile_last_row - W + 1 ||
+                                         (!kCausal && k0 + kTileRows - 1 > tile_first_row + W - 1));
             const bool tile_mask = (k0 + kTileRows > L) ||
-                                   (kCausal && k0 + kTileRows - 1 > tile_first_row);
-            // columns >= lim of this row are masked (only on masked tiles)
-            const int lim = tile_mask ? (kCausal ? min(L, row + 1) : L) - k0 : kTileRows;
+                                   (kCausal && k0 + kTileRows - 1 > tile_first_row) || wmask;
+            // columns >= lim and < lo of this row are masked (only on masked tiles)
+            int lim = tile_mask ? (kCausal ? min(L, row + 1) : L) - k0 : kTileRows;
+            int lo = 0;
+            if (wmask) {
+                lo = row - W + 1 - k0;
+                if (!kCausal) lim = min(lim, row + W - k0);
+            }
 
             // ---- pass 1: row max (S read from TMEM, eight independent chains) ----
             float mx;
@@ -359,7 +383,7 @@ __global__ void __launch_bounds__(320, 1)
                 if (tile_mask) {
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
-                        if (c >= lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+                        if (c >= lim || c < lo) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
                 }
                 float mp[8];
 #pragma unroll
@@ -402,7 +426,7 @@ __global__ void __launch_bounds__(320, 1)
                 if (tile_mask) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        if (32 * cc + e >= lim) sv[e] = __float_as_uint(-INFINITY);
+                        if (32 * cc + e >= lim || 32 * cc + e < lo) sv[e] = __float_as_uint(-INFINITY);
                 }
                 if constexpr (!kTF32) {
                     // exp2 arguments two at a time (paired FMA); the row sum adds
@@ -470,7 +494,7 @@ __global__ void __launch_bounds__(320, 1)
                 rowsum = (a0 + a1) + (a2 + a3);
             }
             l = l * alpha + rowsum;
-            if (warp_rescale && j > 0) {   // O row *= alpha (PV of block j-1 is complete)
+            if (warp_rescale && j > jlo(t)) {   // O row *= alpha (PV of block j-1 is complete)
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -544,11 +568,11 @@ __global__ void __launch_bounds__(320, 1)
         atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_DEVICE_TIMEOUT));
 }
 
-template <int D, bool kTF32, bool kF16, bool kCausal, bool kDropout>
+template <int D, bool kTF32, bool kF16, bool kCausal, bool kDropout, bool kWindow>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const FwdParams& p, cudaStream_t stream) {
     using C = FwdCfg<D, kTF32, kF16>;
-    auto kern = attn_fwd_kernel<D, kTF32, kF16, kCausal, kDropout>;
+    auto kern = attn_fwd_kernel<D, kTF32, kF16, kCausal, kDropout, kWindow>;
     static bool configured = false;   // benign race: the attribute call is idempotent
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -560,14 +584,21 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     return cudaGetLastError();
 }
 
+template <int D, bool kTF32, bool kF16, bool kWindow>
+cudaError_t dispatch_mask_w(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdParams& p, bool causal, bool dropout, cudaStream_t s) {
+    if (causal)
+        return dropout ? launch_fwd_t<D, kTF32, kF16, true, true, kWindow>(tq, tk, tv, p, s)
+                       : launch_fwd_t<D, kTF32, kF16, true, false, kWindow>(tq, tk, tv, p, s);
+    return dropout ? launch_fwd_t<D, kTF32, kF16, false, true, kWindow>(tq, tk, tv, p, s)
+                   : launch_fwd_t<D, kTF32, kF16, false, false, kWindow>(tq, tk, tv, p, s);
+}
+
 template <int D, bool kTF32, bool kF16>
 cudaError_t dispatch_mask(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const FwdParams& p, bool causal, bool dropout, cudaStream_t s) {
-    if (causal)
-        return dropout ? launch_fwd_t<D, kTF32, kF16, true, true>(tq, tk, tv, p, s)
-                       : launch_fwd_t<D, kTF32, kF16, true, false>(tq, tk, tv, p, s);
-    return dropout ? launch_fwd_t<D, kTF32, kF16, false, true>(tq, tk, tv, p, s)
-                   : launch_fwd_t<D, kTF32, kF16, false, false>(tq, tk, tv, p, s);
+    return p.window > 0 ? dispatch_mask_w<D, kTF32, kF16, true>(tq, tk, tv, p, causal, dropout, s)
+                        : dispatch_mask_w<D, kTF32, kF16, false>(tq, tk, tv, p, causal, dropout, s);
 }
 
 }  // namespace

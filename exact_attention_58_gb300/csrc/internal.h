@@ -25,6 +25,7 @@ struct FwdParams {
     float out_scale;          // 1 / (1 - dropout_p)
     uint32_t drop_threshold;  // floor(p * 2^32), clamped
     uint32_t seed_lo, seed_hi;
+    int window;               // > 0: sliding window of this many keys
 };
 
 struct BwdParams {
@@ -42,6 +43,7 @@ struct BwdParams {
     float drop_scale;         // 1 / (1 - dropout_p)
     uint32_t drop_threshold;
     uint32_t seed_lo, seed_hi;
+    int window;               // > 0: sliding window of this many keys
 };
 
 // Tensor map over a contiguous [B*H][N][d] array, 128-row boxes of 128 bytes

@@ -79,6 +79,7 @@ class Inputs:
     causal: bool
     dropout_p: float
     seed: int
+    window: int = 0   # > 0: sliding window of this many keys
 
 
 def make_inputs(B: int, H: int, N: int, d: int, *, dtype=torch.bfloat16, sigma: float = 1.0,

@@ -34,7 +34,10 @@
  *             ATTN_ERR_INVALID_ARG: the library never falls back to another
  *             implementation.
  *  Mask       key j of sequence b is attended iff j < key_lens[b] (all N keys
- *             when key_lens is NULL) and, when causal != 0, j <= i.  A query
+ *             when key_lens is NULL), when causal != 0, j <= i, and, when
+ *             window > 0 (sliding-window attention), i - j < window and, unless
+ *             causal, j - i < window; window <= 0 means no window.  Key blocks
+ *             outside the window are skipped, not computed and masked.  A query
  *             row with no valid key gets O = 0 and LSE = -inf (and zero
  *             gradients).  key_lens values outside [0, N] are clamped on the
  *             device and reported as ATTN_ERR_INVALID_ARG through dev_status.
@@ -96,7 +99,7 @@ typedef enum {
  * products) with d = 64.
  */
 attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                     int B, int H, int N, int d, attn_dtype dtype, float scale, int causal,
+                     int B, int H, int N, int d, attn_dtype dtype, float scale, int causal, int window,
                      const int32_t* key_lens, float dropout_p, uint64_t seed,
                      int* dev_status, void* stream);
 
@@ -117,7 +120,7 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d);
  */
 attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
                      const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
-                     int B, int H, int N, int d, attn_dtype dtype, float scale, int causal,
+                     int B, int H, int N, int d, attn_dtype dtype, float scale, int causal, int window,
                      const int32_t* key_lens, float dropout_p, uint64_t seed,
                      void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
 
@@ -136,7 +139,7 @@ attn_status attn_bwd_preprocess(const void* O, const void* dO, const float* LSE,
                                 void* workspace, size_t workspace_bytes, void* stream);
 attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO,
                           void* dK, void* dV, int B, int H, int N, int d, attn_dtype dtype,
-                          float scale, int causal, const int32_t* key_lens, float dropout_p,
+                          float scale, int causal, int window, const int32_t* key_lens, float dropout_p,
                           uint64_t seed, void* workspace, size_t workspace_bytes,
                           int* dev_status, void* stream);
 attn_status attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, attn_dtype dtype,
@@ -165,7 +168,7 @@ attn_status attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, attn_dtype
 attn_status attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
                              const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
                              int B, int H, int N, int d, attn_dtype dtype, float scale,
-                             int causal, const int32_t* key_lens, float dropout_p,
+                             int causal, int window, const int32_t* key_lens, float dropout_p,
                              uint64_t seed, int* dev_status, void* stream);
 
 /* Static, NUL-terminated description of a status code. */

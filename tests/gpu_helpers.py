@@ -29,7 +29,7 @@ def gpu_fwd(inp):
     q, k, v, _, kl = to_dev(inp)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     o, lse = ea.attn_fwd(q, k, v, causal=inp.causal, key_lens=kl, dropout_p=inp.dropout_p,
-                         seed=inp.seed, scale=inp.scale, dev_status=status)
+                         seed=inp.seed, scale=inp.scale, dev_status=status, window=inp.window)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     return o, lse
@@ -39,10 +39,10 @@ def gpu_fwd_bwd(inp):
     q, k, v, do, kl = to_dev(inp)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     o, lse = ea.attn_fwd(q, k, v, causal=inp.causal, key_lens=kl, dropout_p=inp.dropout_p,
-                         seed=inp.seed, scale=inp.scale, dev_status=status)
+                         seed=inp.seed, scale=inp.scale, dev_status=status, window=inp.window)
     dq, dk, dv = ea.attn_bwd(q, k, v, o, do, lse, causal=inp.causal, key_lens=kl,
                              dropout_p=inp.dropout_p, seed=inp.seed, scale=inp.scale,
-                             dev_status=status)
+                             dev_status=status, window=inp.window)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     return o, lse, dq, dk, dv
@@ -55,13 +55,13 @@ def f64(t):
 def oracle_fwd(inp):
     kl = None if inp.key_lens is None else inp.key_lens.numpy()
     return oracle.attn_fwd(f64(inp.q), f64(inp.k), f64(inp.v), inp.scale, inp.causal, kl,
-                           inp.dropout_p, inp.seed)
+                           inp.dropout_p, inp.seed, window=inp.window)
 
 
 def oracle_bwd(inp):
     kl = None if inp.key_lens is None else inp.key_lens.numpy()
     return oracle.attn_bwd(f64(inp.q), f64(inp.k), f64(inp.v), f64(inp.do), inp.scale,
-                           inp.causal, kl, inp.dropout_p, inp.seed)
+                           inp.causal, kl, inp.dropout_p, inp.seed, window=inp.window)
 
 
 def lse_err(lse, lse_ref):

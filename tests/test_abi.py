@@ -52,11 +52,12 @@ FAKE = 0x10000  # 16-byte aligned, never dereferenced: every case fails validati
 
 def _fwd(lib, **kw):
     a = dict(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, LSE=FAKE, B=1, H=1, N=128, d=64, dtype=0,
-             scale=0.125, causal=0, key_lens=None, p=0.0, seed=0, dev_status=None, stream=None)
+             scale=0.125, causal=0, window=0, key_lens=None, p=0.0, seed=0, dev_status=None,
+             stream=None)
     a.update(kw)
     return lib.attn_fwd(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["H"], a["N"],
-                        a["d"], a["dtype"], a["scale"], a["causal"], a["key_lens"], a["p"],
-                        a["seed"], a["dev_status"], a["stream"])
+                        a["d"], a["dtype"], a["scale"], a["causal"], a["window"], a["key_lens"],
+                        a["p"], a["seed"], a["dev_status"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,expected", [
@@ -88,7 +89,7 @@ def _bwd(lib, **kw):
              ptrs=[FAKE] * 9)
     a.update(kw)
     return lib.attn_bwd(*a["ptrs"], a["B"], a["H"], a["N"], a["d"], a["dtype"], a["scale"], 0,
-                        None, a["p"], 0, a["ws"], a["ws_bytes"], None, None)
+                        0, None, a["p"], 0, a["ws"], a["ws_bytes"], None, None)
 
 
 @pytest.mark.parametrize("kw,expected", [
