@@ -73,8 +73,9 @@ def _bind(lib):
     lib.oracle_heads_fwd.restype = ctypes.c_int
     lib.oracle_heads_bwd.argtypes = [_dp] * 8 + heads_common
     lib.oracle_heads_bwd.restype = ctypes.c_int
-    lib.oracle_heads_rows_fwd_bwd.argtypes = (
-        [_dp] * 4 + [ctypes.c_int, _ip, _ip, _ip, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+    lib.oracle_heads_rows_fwd_bwd.argtypes = (   # ..., key_len, Nq, Nk, d, scale, ...
+        [_dp] * 4 + [ctypes.c_int, _ip, _ip, _ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                     ctypes.c_double,
                      ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_uint64, ctypes.c_int,
                      ctypes.c_int]
         + [_dp] * 5 + [ctypes.c_int])
@@ -273,28 +274,53 @@ def heads_rows_fwd_bwd(Qh, Kh, Vh, dOh, b_idx, h_idx, key_len, scale, row0, nrow
                        causal=False, dropout_p=0.0, seed=0, nthreads=0, window=0, _lib=None):
     """Forward and backward of query rows [row0, row0+nrows) of selected heads.
 
-    Returns O_rows, LSE_rows, dQ_rows ([nh, nrows, ...]) and the rows'
-    contributions to dK and dV ([nh, N, d])."""
+    Qh, dOh are [nh, Nq, d] and Kh, Vh [nh, Nk, d]; Nq != Nk aligns the
+    queries with the last keys (see oracle.c).  Returns O_rows, LSE_rows,
+    dQ_rows ([nh, nrows, ...]) and the rows' contributions to dK and dV
+    ([nh, Nk, d])."""
     L = _lib or lib()
     Qh, Kh, Vh, dOh = _f64(Qh), _f64(Kh), _f64(Vh), _f64(dOh)
     nh, N, d = Qh.shape
+    Nk = Kh.shape[1]
     b_idx = np.ascontiguousarray(b_idx, dtype=np.int32)
     h_idx = np.ascontiguousarray(h_idx, dtype=np.int32)
     key_len = np.ascontiguousarray(key_len, dtype=np.int32)
     O = np.zeros((nh, nrows, d))
     LSE = np.zeros((nh, nrows))
     dQ = np.zeros((nh, nrows, d))
-    dK = np.zeros((nh, N, d))
-    dV = np.zeros((nh, N, d))
+    dK = np.zeros((nh, Nk, d))
+    dV = np.zeros((nh, Nk, d))
     r = L.oracle_heads_rows_fwd_bwd(_ptr(Qh, _dp), _ptr(Kh, _dp), _ptr(Vh, _dp), _ptr(dOh, _dp),
                                     nh, _ptr(b_idx, _ip), _ptr(h_idx, _ip), _ptr(key_len, _ip),
-                                    N, d, float(scale), int(bool(causal)), int(window), float(dropout_p),
+                                    N, Nk, d, float(scale), int(bool(causal)), int(window), float(dropout_p),
                                     int(seed), int(row0), int(nrows), _ptr(O, _dp),
                                     _ptr(LSE, _dp), _ptr(dQ, _dp), _ptr(dK, _dp), _ptr(dV, _dp),
                                     int(nthreads))
     if r != 0:
         raise ValueError("oracle_heads_rows_fwd_bwd rejected its arguments")
     return O, LSE, dQ, dK, dV
+
+
+def attn_fwd_bwd_qk(Q, K, V, dO, scale=None, causal=False, key_lens=None, dropout_p=0.0,
+                    seed=0, window=0, nthreads=0, _lib=None):
+    """Forward and backward for Q, dO [B,H,Nq,d] and K, V [B,H,Nk,d], Nq and
+    Nk free (cross-attention, queries aligned with the last keys).  Returns
+    O, LSE, dQ, dK, dV."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    kl = _key_lens(key_lens, B, Nk)
+    b_idx = np.repeat(np.arange(B, dtype=np.int32), H)
+    h_idx = np.tile(np.arange(H, dtype=np.int32), B)
+    klh = np.repeat(kl, H).astype(np.int32)
+    O, LSE, dQ, dK, dV = heads_rows_fwd_bwd(
+        Q.reshape(B * H, Nq, d), K.reshape(B * H, Nk, d), V.reshape(B * H, Nk, d),
+        dO.reshape(B * H, Nq, d), b_idx, h_idx, klh, scale, 0, Nq, causal=causal,
+        dropout_p=dropout_p, seed=seed, nthreads=nthreads, window=window, _lib=_lib)
+    return (O.reshape(B, H, Nq, d), LSE.reshape(B, H, Nq), dQ.reshape(B, H, Nq, d),
+            dK.reshape(B, H, Nk, d), dV.reshape(B, H, Nk, d))
 
 
 def num_threads() -> int:

@@ -329,18 +329,27 @@ int oracle_head_fwd_rows(const double* q, const double* k, const double* v,
 
 /*
  * Forward and backward of the query rows [row0, row0 + nrows) of one head,
- * row by row, without an N x N array: O, LSE and dQ of those rows, and the
- * rows' contributions to dK and dV added into dk_part and dv_part ([N][d],
+ * row by row, without an Nq x Nk array: O, LSE and dQ of those rows, and the
+ * rows' contributions to dK and dV added into dk_part and dv_part ([Nk][d],
  * zeroed by the caller).  The same definitions as oracle_head_fwd and
  * oracle_head_bwd, restricted to a slice of the rows; summed over a partition
  * of all rows, the contributions give the head's dK and dV.
+ *
+ * Nq query rows and Nk keys may differ (cross-attention).  Queries are then
+ * aligned with the last keys: query i plays the part of position i + Nk - Nq
+ * in the causal and window tests, so the last query sees every key when
+ * causal (the usual convention when a shorter query block continues a longer
+ * key sequence).  With Nq == Nk this is the square definition.
  */
 int oracle_head_rows_fwd_bwd(const double* q, const double* k, const double* v,
                              const double* dout, int row0, int nrows, double* o_rows,
                              double* lse_rows, double* dq_rows, double* dk_part, double* dv_part,
-                             int N, int d, double scale, int causal, int window, int key_len, double p,
-                             uint64_t seed, int b, int h) {
-    if (check_args(N, d, p, key_len) || row0 < 0 || nrows < 0 || row0 + nrows > N) return -1;
+                             int Nq, int Nk, int d, double scale, int causal, int window,
+                             int key_len, double p, uint64_t seed, int b, int h) {
+    if (check_args(Nk, d, p, key_len) || Nq < 1 || row0 < 0 || nrows < 0 || row0 + nrows > Nq)
+        return -1;
+    const int N = Nk;          /* keys */
+    const int off = Nk - Nq;   /* query i sits at position i + off */
     double* P = (double*)malloc(sizeof(double) * (size_t)N);
     double* F = (double*)malloc(sizeof(double) * (size_t)N);
     if (!P || !F) { free(P); free(F); return -2; }
@@ -356,7 +365,7 @@ int oracle_head_rows_fwd_bwd(const double* q, const double* k, const double* v,
         double m = -INFINITY;
         for (int j = 0; j < N; ++j) {
             double sc = -INFINITY;
-            if (valid_pair(i, j, causal, window, key_len)) {
+            if (valid_pair(i + off, j, causal, window, key_len)) {
                 double acc = 0.0;
                 for (int c = 0; c < d; ++c) acc += qi[c] * k[(size_t)j * d + c];
                 sc = scale * acc;
@@ -402,12 +411,12 @@ int oracle_head_rows_fwd_bwd(const double* q, const double* k, const double* v,
     return 0;
 }
 
-/* Rows [row0, row0 + nrows) of nh heads (OpenMP over heads); array layout as in
- * oracle_heads_fwd, with *_rows arrays [nh][nrows](...) and the partial dK,
- * dV arrays [nh][N][d] (zeroed here). */
+/* Rows [row0, row0 + nrows) of nh heads (OpenMP over heads); Q, dO are
+ * [nh][Nq][d], K, V [nh][Nk][d], the *_rows arrays [nh][nrows](...) and the
+ * partial dK, dV arrays [nh][Nk][d] (zeroed here). */
 int oracle_heads_rows_fwd_bwd(const double* Q, const double* K, const double* V,
                               const double* dO, int nh, const int32_t* b_idx,
-                              const int32_t* h_idx, const int32_t* key_len, int N, int d,
+                              const int32_t* h_idx, const int32_t* key_len, int Nq, int Nk, int d,
                               double scale, int causal, int window, double p, uint64_t seed, int row0,
                               int nrows, double* O_rows, double* LSE_rows, double* dQ_rows,
                               double* dK_part, double* dV_part, int nthreads);
@@ -542,21 +551,22 @@ int oracle_heads_bwd(const double* Q, const double* K, const double* V, const do
 
 int oracle_heads_rows_fwd_bwd(const double* Q, const double* K, const double* V,
                               const double* dO, int nh, const int32_t* b_idx,
-                              const int32_t* h_idx, const int32_t* key_len, int N, int d,
+                              const int32_t* h_idx, const int32_t* key_len, int Nq, int Nk, int d,
                               double scale, int causal, int window, double p, uint64_t seed, int row0,
                               int nrows, double* O_rows, double* LSE_rows, double* dQ_rows,
                               double* dK_part, double* dV_part, int nthreads) {
     if (nh < 0) return -1;
     set_threads(nthreads);
     int err = 0;
-    size_t hd = (size_t)N * d, rd = (size_t)nrows * d;
+    size_t qd = (size_t)Nq * d, kd = (size_t)Nk * d, rd = (size_t)nrows * d;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
     for (int x = 0; x < nh; ++x) {
-        for (size_t y = 0; y < hd; ++y) { dK_part[x * hd + y] = 0.0; dV_part[x * hd + y] = 0.0; }
-        int r = oracle_head_rows_fwd_bwd(Q + x * hd, K + x * hd, V + x * hd, dO + x * hd, row0,
+        for (size_t y = 0; y < kd; ++y) { dK_part[x * kd + y] = 0.0; dV_part[x * kd + y] = 0.0; }
+        int r = oracle_head_rows_fwd_bwd(Q + x * qd, K + x * kd, V + x * kd, dO + x * qd, row0,
                                          nrows, O_rows + x * rd, LSE_rows + (size_t)x * nrows,
-                                         dQ_rows + x * rd, dK_part + x * hd, dV_part + x * hd, N, d,
-                                         scale, causal, window, key_len[x], p, seed, b_idx[x], h_idx[x]);
+                                         dQ_rows + x * rd, dK_part + x * kd, dV_part + x * kd, Nq,
+                                         Nk, d, scale, causal, window, key_len[x], p, seed, b_idx[x],
+                                         h_idx[x]);
         if (r) err |= 1;
     }
     return err ? -1 : 0;

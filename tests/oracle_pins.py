@@ -232,6 +232,50 @@ def pin_window_torch(L) -> float:
     return worst
 
 
+def pin_cross_attention_torch(L) -> float:
+    """Nq != Nk (queries aligned with the last keys: query i stands at key
+    position i + Nk - Nq) against torch float64 with the rectangular mask
+    written out, forward and autograd backward, with padding, dropout and a
+    window; more queries than keys leaves the first Nq - Nk rows empty under
+    the causal mask (O = 0, LSE = -inf, zero gradients)."""
+    worst = 0.0
+    for Nq, Nk, d, causal, key_len, p, w in ((5, 13, 4, True, 13, 0.0, 0), (13, 5, 8, True, 5, 0.0, 0),
+                                              (7, 11, 4, False, 9, 0.25, 0), (9, 16, 8, True, 14, 0.0, 4),
+                                              (1, 10, 4, True, 10, 0.0, 0)):
+        B, H = 1, 2
+        q, do = _rand(B, H, Nq, d), _rand(B, H, Nq, d)
+        k, v = _rand(B, H, Nk, d), _rand(B, H, Nk, d)
+        sc = 1 / math.sqrt(d)
+        O, LSE, dQ, dK, dV = oracle.attn_fwd_bwd_qk(q, k, v, do, sc, causal, [key_len], p, 7,
+                                                    window=w, _lib=L)
+        i = np.arange(Nq)[:, None] + (Nk - Nq)
+        j = np.arange(Nk)[None, :]
+        valid = np.broadcast_to(j < key_len, (Nq, Nk)).copy()
+        if causal:
+            valid &= j <= i
+        if w > 0:
+            valid &= i - j < w
+            if not causal:
+                valid &= j - i < w
+        for h in range(H):
+            tq, tk, tv = (torch.tensor(a[0, h], requires_grad=True) for a in (q, k, v))
+            s_ = (sc * tq @ tk.T).masked_fill(~torch.as_tensor(valid), float("-inf"))
+            tl = torch.logsumexp(s_, dim=-1)
+            P = torch.nan_to_num(torch.softmax(s_, dim=-1), nan=0.0)
+            if p > 0:
+                Z = oracle.dropout_mask(7, 0, h, Nq, Nk, p, _lib=L)
+                P = P * torch.as_tensor(Z, dtype=torch.float64) / (1 - p)
+            to = P @ tv
+            (to * torch.tensor(do[0, h])).sum().backward()
+            worst = max(worst, np.abs(O[0, h] - to.detach().numpy()).max())
+            fin = np.isfinite(LSE[0, h])
+            worst = max(worst, np.abs(LSE[0, h][fin] - tl.detach().numpy()[fin]).max())
+            worst = max(worst, float((~fin != ~np.isfinite(tl.detach().numpy())).any()))
+            for g, tg in ((dQ, tq), (dK, tk), (dV, tv)):
+                worst = max(worst, np.abs(g[0, h] - tg.grad.numpy()).max())
+    return worst
+
+
 def pin_philox_vs_triton(L) -> float:
     """The oracle's Philox4x32-10 against Triton's implementation of the same
     generator (run by Triton's CPU interpreter in a child process).  Returns
@@ -428,6 +472,7 @@ PINS = {
     "torch_autograd": (pin_torch_autograd, 1e-12),
     "window_one": (pin_window_one, 1e-12),
     "window_torch": (pin_window_torch, 1e-12),
+    "cross_attention_torch": (pin_cross_attention_torch, 1e-12),
     "finite_differences": (pin_finite_differences, 1e-6),
     "dk_sums_to_zero": (pin_dk_sums_to_zero, 1e-12),
     "D_equals_dO_dot_O": (pin_D_equals_dO_dot_O, 1e-12),

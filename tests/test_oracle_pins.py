@@ -58,6 +58,8 @@ MUTATIONS = {
     "causal_off_by_one": ("if (causal && j > i) return 0;", "if (causal && j >= i) return 0;"),
     "window_off_by_one": ("if (i - j >= window) return 0;", "if (i - j > window) return 0;"),
     "window_one_sided": ("if (!causal && j - i >= window) return 0;", "if (0) return 0;"),
+    "cross_offset_sign": ("if (valid_pair(i + off, j, causal, window, key_len)) {",
+                          "if (valid_pair(i - off, j, causal, window, key_len)) {"),
     "scores_unscaled": ("                s = scale * acc;\n", "                s = acc;\n"),
     "dropout_no_rescale": ("oracle_dropout_keep(seed, b, h, i, j, t) ? inv : 0.0;",
                            "oracle_dropout_keep(seed, b, h, i, j, t) ? 1.0 : 0.0;"),
