@@ -43,14 +43,19 @@ L2_BYTES = 129 * 2**20
 # ---------------------------------------------------------------------------
 # algorithmic work
 # ---------------------------------------------------------------------------
-def window_flops_fwd(w: Workload, window: int) -> float:
-    """4 d FLOPs per attended (query, key) pair under a sliding window of
-    `window` keys (causal: i - window < j <= i; else |i - j| < window)."""
-    i = np.arange(w.N)
-    if w.causal:
-        pairs = np.minimum(i + 1, window).sum()
-    else:
-        pairs = (np.minimum(i + window, w.N) - np.maximum(0, i - window + 1)).sum()
+def pairs_flops_fwd(w: Workload, window: int, Nk: int) -> float:
+    """4 d FLOPs per attended (query, key) pair, counted exactly: query i
+    stands at key position t = i + Nk - N; key j < Nk is attended when j <= t
+    (causal) and t - j < window (and j - t < window unless causal) for a
+    window > 0."""
+    t = np.arange(w.N, dtype=np.int64) + (Nk - w.N)
+    hi = np.minimum(t + 1, Nk) if w.causal else np.full_like(t, Nk)
+    lo = np.zeros_like(t)
+    if window > 0:
+        lo = np.maximum(0, t - window + 1)
+        if not w.causal:
+            hi = np.minimum(hi, t + window)
+    pairs = np.maximum(0, hi - lo).sum()
     return 4.0 * w.B * w.H * w.d * float(pairs)
 
 
@@ -277,7 +282,8 @@ def run_ours(args, w: Workload):
     torch.cuda.set_device(dev)
     ea.library()
 
-    inp = make_workload_inputs(args.workload)
+    Nk = args.nk if args.nk > 0 else w.N
+    inp = make_workload_inputs(args.workload, Nk=Nk)
     if args.dtype == "fp16":   # the same draws stored as IEEE half
         for name in ("q", "k", "v", "do"):
             t = getattr(inp, name)
@@ -291,7 +297,7 @@ def run_ours(args, w: Workload):
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     if bwd:
-        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
         ws = torch.empty(ea.attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     kw = dict(causal=w.causal, window=args.window, key_lens=kl, dropout_p=inp.dropout_p, seed=inp.seed,
@@ -319,7 +325,8 @@ def run_ours(args, w: Workload):
     # Inputs that fit in L2 would be served from it on every step; then L2 is
     # flushed (a 256 MiB write) before each step, outside the per-stage
     # events, and the step time is the sum of the stage times.
-    in_bytes = (4 if bwd else 3) * q.numel() * q.element_size()
+    qbytes, kbytes = q.numel() * q.element_size(), k.numel() * k.element_size()
+    in_bytes = (2 if bwd else 1) * qbytes + 2 * kbytes
     flush = in_bytes <= L2_BYTES
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush else None
 
@@ -359,7 +366,8 @@ def run_ours(args, w: Workload):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
 
-    flops_fwd = w.flops_fwd() if args.window <= 0 else window_flops_fwd(w, args.window)
+    exact = args.window > 0 or Nk != w.N
+    flops_fwd = pairs_flops_fwd(w, args.window, Nk) if exact else w.flops_fwd()
     flops_bwd = (2.5 * flops_fwd) if bwd else 0.0
     flops_step = flops_fwd + flops_bwd
     value = world * flops_step * args.steps / (elapsed_ms * 1e-3) / 1e12
@@ -386,7 +394,8 @@ def run_ours(args, w: Workload):
     if args.e2e_steps > 0:
         hq, hk, hv = (t.pin_memory() for t in (inp.q, inp.k, inp.v))
         hdo = inp.do.pin_memory() if bwd else None
-        ho, hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(4))
+        ho, hdq = torch.empty_like(hq).pin_memory(), torch.empty_like(hq).pin_memory()
+        hdk, hdv = torch.empty_like(hk).pin_memory(), torch.empty_like(hk).pin_memory()
         s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
         def e2e_step():
@@ -413,15 +422,14 @@ def run_ours(args, w: Workload):
         e_ev.record()
         torch.cuda.synchronize()
         e_ms = s_ev.elapsed_time(e_ev)
-        nbytes = q.numel() * q.element_size()
         e2e = {"value": flops_step * args.e2e_steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": (4 if bwd else 3) * nbytes,
-               "d2h_bytes_per_step": (4 if bwd else 1) * nbytes,
+               "h2d_bytes_per_step": in_bytes,
+               "d2h_bytes_per_step": (2 * qbytes + 2 * kbytes) if bwd else qbytes,
                "ms_per_step": e_ms / args.e2e_steps}
 
     cpu = None
     # the sample is forward+backward of the default (unwindowed) configuration
-    if world == 1 and not args.no_cpu_baseline and bwd and args.window <= 0:
+    if world == 1 and not args.no_cpu_baseline and bwd and not exact:
         cpu = cpu_baseline(inp, w, target_s=args.cpu_seconds)
 
     l2_note = (f"inputs {in_bytes / 2**20:.0f} MiB <= L2: L2 flushed (256 MiB write) before every step"
@@ -436,6 +444,7 @@ def run_ours(args, w: Workload):
                    "causal": w.causal, "dropout_p": w.dropout_p,
                    "passes": "fwd+bwd" if bwd else "fwd",
                    "window": args.window if args.window > 0 else None,
+                   "Nk": Nk if Nk != w.N else None,
                    "global_batch": world * w.B, "seq_len": w.N,
                    "parallelism": f"replicas x{world} (heads independent)",
                    "l2": l2_note},
@@ -461,6 +470,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window of this many keys (FLOPs count the attended pairs exactly)")
+    ap.add_argument("--nk", type=int, default=0,
+                    help="cross-attention: this many keys (queries are the last N positions)")
     ap.add_argument("--dtype", choices=["default", "fp16"], default="default",
                     help="fp16: store the workload's inputs as IEEE half (16-bit workloads only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

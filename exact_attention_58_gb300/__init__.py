@@ -10,8 +10,9 @@ unsupported, the call raises.
     o, lse = ea.attn_fwd(q, k, v, causal=True)
     dq, dk, dv = ea.attn_bwd(q, k, v, o, do, lse, causal=True)
 
-Tensors are [B, H, N, d], contiguous, on one CUDA device; bf16 (d = 64 or
-128) or, forward only, fp32 with d = 64.
+q, o, do, dq are [B, H, N, d] and k, v, dk, dv [B, H, Nk, d] (Nk = N for
+self-attention), contiguous, on one CUDA device; bf16 or fp16 (d = 64 or 128)
+or, forward only, fp32 with d = 64.
 """
 from __future__ import annotations
 
@@ -69,17 +70,14 @@ def library():
             lib = ctypes.CDLL(LIB_PATH)
             vp, ip, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
             f, u64 = ctypes.c_float, ctypes.c_uint64
-            lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, f, ip, ip, vp, f, u64,
-                                     vp, vp]
-            lib.attn_bwd.argtypes = [vp] * 9 + [ip, ip, ip, ip, ip, f, ip, ip, vp, f, u64, vp, sz,
-                                                vp, vp]
-            lib.attn_bwd_noalloc.argtypes = [vp] * 9 + [ip, ip, ip, ip, ip, f, ip, ip, vp, f, u64,
-                                                        vp, vp]
+            lib.attn_fwd.argtypes = [vp] * 5 + [ip] * 6 + [f, ip, ip, vp, f, u64, vp, vp]
+            lib.attn_bwd.argtypes = [vp] * 9 + [ip] * 6 + [f, ip, ip, vp, f, u64, vp, sz, vp, vp]
+            lib.attn_bwd_noalloc.argtypes = [vp] * 9 + [ip] * 6 + [f, ip, ip, vp, f, u64, vp, vp]
             lib.attn_bwd_workspace_size.argtypes = [ip, ip, ip, ip]
             lib.attn_bwd_workspace_size.restype = sz
             lib.attn_bwd_preprocess.argtypes = [vp, vp, vp, ip, ip, ip, ip, ip, vp, sz, vp]
-            lib.attn_bwd_main.argtypes = [vp] * 6 + [ip, ip, ip, ip, ip, f, ip, ip, vp, f, u64, vp,
-                                                     sz, vp, vp]
+            lib.attn_bwd_main.argtypes = [vp] * 6 + [ip] * 6 + [f, ip, ip, vp, f, u64, vp, sz, vp,
+                                                              vp]
             lib.attn_bwd_dq_convert.argtypes = [vp, ip, ip, ip, ip, ip, f, vp, sz, vp]
             for fn in ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
                        "attn_bwd_dq_convert", "attn_bwd_noalloc"):
@@ -132,6 +130,16 @@ def _check_like(name: str, t: torch.Tensor, ref: torch.Tensor):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _keys(q: torch.Tensor, k: torch.Tensor) -> int:
+    """Nk of k, which must be [B, H, Nk, d] like q apart from its length."""
+    if (k.dim() != 4 or k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]
+            or k.dtype != q.dtype or k.device != q.device):
+        raise ValueError("k must be [B, H, Nk, d] with q's B, H, d, dtype and device")
+    if not k.is_contiguous():
+        raise ValueError("k must be contiguous")
+    return int(k.shape[2])
+
+
 def _dtype_code(t: torch.Tensor) -> int:
     if t.dtype not in _DTYPE:
         raise ValueError(f"unsupported dtype {t.dtype}")
@@ -162,8 +170,8 @@ def attn_fwd(q, k, v, *, causal: bool = False, window: int = 0, key_lens=None,
     """O, LSE = attention(q, k, v); see include/gbattn.h for the exact contract."""
     B, H, N, d = _shape(q)
     _check_like("q", q, q)
-    _check_like("k", k, q)
-    _check_like("v", v, q)
+    Nk = _keys(q, k)
+    _check_like("v", v, k)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
@@ -172,7 +180,7 @@ def attn_fwd(q, k, v, *, causal: bool = False, window: int = 0, key_lens=None,
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     kl = _key_lens(key_lens, q)
-    st = library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
+    st = library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, Nk, d,
                             _dtype_code(q), float(scale), int(bool(causal)), int(window), _ptr(kl),
                             float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(dev_status),
                             _stream(stream))
@@ -192,19 +200,22 @@ def attn_bwd(q, k, v, o, do, lse, *, causal: bool = False, window: int = 0, key_
              dk=None, dv=None, workspace=None, dev_status=None, stream=None):
     """dQ, dK, dV of attention given the forward's o and lse and the gradient do."""
     B, H, N, d = _shape(q)
-    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+    Nk = _keys(q, k)
+    for name, t in (("o", o), ("do", do)):
         _check_like(name, t, q)
+    _check_like("v", v, k)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
-    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-        _check_like(name, t, q)
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(k) if dv is None else dv
+    _check_like("dq", dq, q)
+    _check_like("dk", dk, k)
+    _check_like("dv", dv, k)
     ws, ws_bytes = _workspace(B, H, N, d, workspace, q.device)
     kl = _key_lens(key_lens, q)
     st = library().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
-                            _ptr(dk), _ptr(dv), B, H, N, d, _dtype_code(q), float(scale),
+                            _ptr(dk), _ptr(dv), B, H, N, Nk, d, _dtype_code(q), float(scale),
                             int(bool(causal)), int(window), _ptr(kl), float(dropout_p),
                             int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(ws), ws_bytes, _ptr(dev_status),
                             _stream(stream))
@@ -220,19 +231,23 @@ def attn_bwd_noalloc(q, k, v, o, do, lse, *, causal: bool = False, window: int =
     workspace, for callers that cannot allocate device memory.  Outputs must be
     passed in (dq, dk, dv) by such callers; see include/gbattn.h."""
     B, H, N, d = _shape(q)
-    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+    Nk = _keys(q, k)
+    for name, t in (("o", o), ("do", do)):
         _check_like(name, t, q)
+    _check_like("v", v, k)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
-    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-        _check_like(name, t, q)
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(k) if dv is None else dv
+    _check_like("dq", dq, q)
+    _check_like("dk", dk, k)
+    _check_like("dv", dv, k)
     kl = _key_lens(key_lens, q)
     st = library().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
-                                    _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, _dtype_code(q),
-                                    float(scale), int(bool(causal)), int(window), _ptr(kl), float(dropout_p),
+                                    _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, Nk, d, _dtype_code(q),
+                                    float(scale), int(bool(causal)), int(window), _ptr(kl),
+                                    float(dropout_p),
                                     int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(dev_status),
                                     _stream(stream))
     _raise(st, "attn_bwd_noalloc")
@@ -252,11 +267,13 @@ def attn_bwd_preprocess(o, do, lse, workspace, *, stream=None):
 def attn_bwd_main(q, k, v, do, dk, dv, workspace, *, causal=False, window=0, key_lens=None,
                   dropout_p=0.0, seed=0, scale=None, dev_status=None, stream=None):
     B, H, N, d = _shape(q)
+    Nk = _keys(q, k)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     kl = _key_lens(key_lens, q)
     st = library().attn_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dk), _ptr(dv), B, H,
-                                 N, d, _dtype_code(q), float(scale), int(bool(causal)), int(window), _ptr(kl),
+                                 N, Nk, d, _dtype_code(q), float(scale), int(bool(causal)),
+                                 int(window), _ptr(kl),
                                  float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF,
                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _ptr(dev_status), _stream(stream))

@@ -42,6 +42,14 @@ attn_status check_shape(int B, int H, int N, int d, attn_dtype dtype, bool backw
     return ATTN_OK;
 }
 
+// Key length of cross-attention: K and V (and dK, dV) hold Nk rows a head.
+attn_status check_keys(int B, int H, int Nk, int d) {
+    if (Nk < 1) return ATTN_ERR_INVALID_ARG;
+    const long long elems = static_cast<long long>(B) * H * npad_of(Nk) * d;
+    if (elems >= (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
 attn_status check_math(float scale, float dropout_p) {
     if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     if (!(dropout_p >= 0.f && dropout_p < 1.f)) return ATTN_ERR_INVALID_ARG;
@@ -110,18 +118,19 @@ using namespace gbattn;
 extern "C" {
 
 attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
-                     int H, int N, int d, attn_dtype dtype, float scale, int causal, int window,
-                     const int32_t* key_lens, float dropout_p, uint64_t seed, int* dev_status,
-                     void* stream) {
+                     int H, int N, int Nk, int d, attn_dtype dtype, float scale, int causal,
+                     int window, const int32_t* key_lens, float dropout_p, uint64_t seed,
+                     int* dev_status, void* stream) {
     if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
     attn_status st = check_shape(B, H, N, d, dtype, false);
     if (st != ATTN_OK) return st;
+    if ((st = check_keys(B, H, Nk, d)) != ATTN_OK) return st;
     if ((st = check_math(scale, dropout_p)) != ATTN_OK) return st;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
         return ATTN_ERR_MISALIGNED;
     CUtensorMap tq, tk, tv;
-    if (!make_tmap_bhnd(&tq, Q, dtype, B * H, N, d) || !make_tmap_bhnd(&tk, K, dtype, B * H, N, d) ||
-        !make_tmap_bhnd(&tv, V, dtype, B * H, N, d))
+    if (!make_tmap_bhnd(&tq, Q, dtype, B * H, N, d) || !make_tmap_bhnd(&tk, K, dtype, B * H, Nk, d) ||
+        !make_tmap_bhnd(&tv, V, dtype, B * H, Nk, d))
         return ATTN_ERR_CUDA;
     FwdParams p{};
     p.V = V;
@@ -132,6 +141,7 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
     p.B = B;
     p.H = H;
     p.N = N;
+    p.Nk = Nk;
     p.nqb = (N + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.out_scale = 1.0f / (1.0f - dropout_p);
@@ -162,23 +172,23 @@ attn_status attn_bwd_preprocess(const void* O, const void* dO, const float* LSE,
 }
 
 attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dK,
-                          void* dV, int B, int H, int N, int d, attn_dtype dtype, float scale,
-                          int causal, int window, const int32_t* key_lens, float dropout_p,
-                          uint64_t seed,
-                          void* workspace, size_t workspace_bytes, int* dev_status,
-                          void* stream) {
+                          void* dV, int B, int H, int N, int Nk, int d, attn_dtype dtype,
+                          float scale, int causal, int window, const int32_t* key_lens,
+                          float dropout_p, uint64_t seed, void* workspace,
+                          size_t workspace_bytes, int* dev_status, void* stream) {
     if (!Q || !K || !V || !dO || !dK || !dV) return ATTN_ERR_INVALID_ARG;
     attn_status st = check_shape(B, H, N, d, dtype, true);
     if (st != ATTN_OK) return st;
+    if ((st = check_keys(B, H, Nk, d)) != ATTN_OK) return st;
     if ((st = check_math(scale, dropout_p)) != ATTN_OK) return st;
     if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != ATTN_OK) return st;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(dK) ||
         !aligned16(dV))
         return ATTN_ERR_MISALIGNED;
     CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-    if (!make_tmap_bhnd(&tq, Q, dtype, B * H, N, d) || !make_tmap_bhnd(&tk, K, dtype, B * H, N, d) ||
-        !make_tmap_bhnd(&tv, V, dtype, B * H, N, d) || !make_tmap_bhnd(&tdo, dO, dtype, B * H, N, d) ||
-        !make_tmap_bhnd(&tdk, dK, dtype, B * H, N, d) || !make_tmap_bhnd(&tdv, dV, dtype, B * H, N, d))
+    if (!make_tmap_bhnd(&tq, Q, dtype, B * H, N, d) || !make_tmap_bhnd(&tk, K, dtype, B * H, Nk, d) ||
+        !make_tmap_bhnd(&tv, V, dtype, B * H, Nk, d) || !make_tmap_bhnd(&tdo, dO, dtype, B * H, N, d) ||
+        !make_tmap_bhnd(&tdk, dK, dtype, B * H, Nk, d) || !make_tmap_bhnd(&tdv, dV, dtype, B * H, Nk, d))
         return ATTN_ERR_CUDA;
     const Workspace w = carve(workspace, B, H, N);
     BwdParams p{};
@@ -192,8 +202,9 @@ attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const voi
     p.B = B;
     p.H = H;
     p.N = N;
+    p.Nk = Nk;
     p.Npad = npad_of(N);
-    p.nkb = (N + kTileRows - 1) / kTileRows;
+    p.nkb = (Nk + kTileRows - 1) / kTileRows;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.scale = scale;
     p.drop_scale = 1.0f / (1.0f - dropout_p);
@@ -222,15 +233,16 @@ attn_status attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, attn_dtype
 }
 
 attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                     const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
-                     attn_dtype dtype, float scale, int causal, int window, const int32_t* key_lens,
-                     float dropout_p, uint64_t seed, void* workspace, size_t workspace_bytes,
-                     int* dev_status, void* stream) {
+                     const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int N, int Nk,
+                     int d, attn_dtype dtype, float scale, int causal, int window,
+                     const int32_t* key_lens, float dropout_p, uint64_t seed, void* workspace,
+                     size_t workspace_bytes, int* dev_status, void* stream) {
     // Validate everything before the first launch so that errors leave the
     // outputs untouched.
     if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
     attn_status st = check_shape(B, H, N, d, dtype, true);
     if (st != ATTN_OK) return st;
+    if ((st = check_keys(B, H, Nk, d)) != ATTN_OK) return st;
     if ((st = check_math(scale, dropout_p)) != ATTN_OK) return st;
     if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != ATTN_OK) return st;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) ||
@@ -239,7 +251,7 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
     if ((st = attn_bwd_preprocess(O, dO, LSE, B, H, N, d, dtype, workspace, workspace_bytes,
                                   stream)) != ATTN_OK)
         return st;
-    if ((st = attn_bwd_main(Q, K, V, dO, dK, dV, B, H, N, d, dtype, scale, causal, window, key_lens,
+    if ((st = attn_bwd_main(Q, K, V, dO, dK, dV, B, H, N, Nk, d, dtype, scale, causal, window, key_lens,
                             dropout_p, seed, workspace, workspace_bytes, dev_status, stream)) !=
         ATTN_OK)
         return st;
@@ -259,6 +271,6 @@ const char* attn_status_string(attn_status status) {
     return "unknown status";
 }
 
-int attn_version(void) { return 100; }
+int attn_version(void) { return 200; }
 
 }  // extern "C"

@@ -206,18 +206,34 @@ __global__ void __launch_bounds__(448, 1)
     int kb, bh;   // causal: key block 0 meets every query block, so rank 0 is heaviest
     grouped_schedule(static_cast<int>(blockIdx.x), BH, p.nkb, bh, kb);
     const int b = bh / p.H, h = bh % p.H;
-    const int N = p.N;
-    int L = N;
+    const int N = p.N;     // query rows
+    const int Nk = p.Nk;   // keys
+    // Queries continue the key sequence: query i stands at key position
+    // i + off for the causal and window tests (off = 0 when N == Nk).
+    const int off = Nk - N;
+    const int nqb = (N + kTileRows - 1) / kTileRows;
+    int L = Nk;
     if (p.key_lens != nullptr) {
         const int raw = p.key_lens[b];
-        L = raw < 0 ? 0 : (raw > N ? N : raw);
+        L = raw < 0 ? 0 : (raw > Nk ? Nk : raw);
         if (raw != L && threadIdx.x == 0 && p.dev_status != nullptr)
             atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_INVALID_ARG));
     }
     const int k0 = kb * kTileRows;
-    const size_t head_off = static_cast<size_t>(bh) * N * D;
-    if (k0 >= L) {   // every key of this block is masked: dK = dV = 0
-        const int rows = min(kTileRows, N - k0);
+    // Query blocks that see some key of this block: from the diagonal on when
+    // causal; a sliding window of W keys also bounds them from the other side.
+    const int W = kWindow ? p.window : 0;   // compile-time 0 without a window
+    int q_begin = kCausal ? max(0, k0 - off) / kTileRows : 0;
+    int q_end = nqb;
+    if (W > 0) {
+        const int last_q = k0 + kTileRows - 1 - off + W - 1;   // last query the block's keys reach
+        q_end = last_q < 0 ? 0 : min(nqb, last_q / kTileRows + 1);
+        if (!kCausal) q_begin = max(0, k0 - off - W + 1) / kTileRows;
+    }
+    const int nq = q_end - q_begin;
+    const size_t head_off = static_cast<size_t>(bh) * Nk * D;   // of dK, dV
+    if (k0 >= L || nq <= 0) {   // no key of this block is attended: dK = dV = 0
+        const int rows = min(kTileRows, Nk - k0);
         const int n16 = rows * D / 8;   // uint4 per tensor
         uint4* dk = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dK) + head_off +
                                              static_cast<size_t>(k0) * D);
@@ -234,16 +250,6 @@ __global__ void __launch_bounds__(448, 1)
             atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_CUDA));
         return;
     }
-    // Query blocks that see some key of this block: from the diagonal on when
-    // causal; a sliding window of W keys also bounds them from the other side.
-    const int W = kWindow ? p.window : 0;   // compile-time 0 without a window
-    int q_begin = kCausal ? kb : 0;
-    int q_end = p.nkb;
-    if (W > 0) {
-        q_end = min(p.nkb, (k0 + kTileRows - 1 + W - 1) / kTileRows + 1);
-        if (!kCausal) q_begin = max(0, k0 - W + 1) / kTileRows;
-    }
-    const int nq = q_end - q_begin;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* bar_kv = bars + 0;
@@ -491,10 +497,11 @@ __global__ void __launch_bounds__(448, 1)
             const float* lse_s = sLSE + stage * kTileRows + 64 * hh;
             const float* d_s = sD + stage * kTileRows + 64 * hh;
             const int q0h = qi * kTileRows + 64 * hh;   // first query of this half
-            const bool diag = kCausal && (qi == kb);
+            // some key of this block lies past some query's causal limit
+            const bool diag = kCausal && (k0 + kTileRows - 1 > qi * kTileRows + off);
             // some (query, key) pair of this block lies outside the window
-            const bool wmask = W > 0 && (qi * kTileRows + kTileRows - 1 - k0 >= W ||
-                                         (!kCausal && k0 + kTileRows - 1 - qi * kTileRows >= W));
+            const bool wmask = W > 0 && (qi * kTileRows + kTileRows - 1 + off - k0 >= W ||
+                                         (!kCausal && k0 + kTileRows - 1 - qi * kTileRows - off >= W));
             // ---- phase 1 (while dP^T is still on the tensor pipe): P from S ----
             // 16-column chunks; the next chunk's TMEM load overlaps this chunk's
             // math.  P (undropped, fp32) stays in registers for phase 2.
@@ -549,8 +556,8 @@ __global__ void __launch_bounds__(448, 1)
                         float x = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), p.scale_log2,
                                                   -lv[2 * e + u]));
                         const int iq = q0h + col;   // query index
-                        const bool valid = row_valid && (!diag || j <= iq) &&
-                                           (!wmask || (iq - j < W && (kCausal || j - iq < W)));
+                        const bool valid = row_valid && (!diag || j <= iq + off) &&
+                                           (!wmask || (iq + off - j < W && (kCausal || j - iq - off < W)));
                         x = valid ? x : 0.f;
                         pr[col] = x;
                         pd[u] = x;

@@ -119,11 +119,15 @@ __global__ void __launch_bounds__(320, 1)
     grouped_schedule(static_cast<int>(blockIdx.x), BH, p.nqb, bh, qb);
     if (kCausal) qb = p.nqb - 1 - qb;   // the last query blocks see the most keys
     const int b = bh / p.H, h = bh % p.H;
-    const int N = p.N;
-    int L = N;
+    const int N = p.N;     // query rows
+    const int Nk = p.Nk;   // keys
+    // Queries continue the key sequence: query i stands at key position
+    // i + off for the causal and window tests (off = 0 when N == Nk).
+    const int off = Nk - N;
+    int L = Nk;
     if (p.key_lens != nullptr) {
         const int raw = p.key_lens[b];
-        L = raw < 0 ? 0 : (raw > N ? N : raw);
+        L = raw < 0 ? 0 : (raw > Nk ? Nk : raw);
         if (raw != L && threadIdx.x == 0 && p.dev_status != nullptr)
             atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_INVALID_ARG));
     }
@@ -142,10 +146,11 @@ __global__ void __launch_bounds__(320, 1)
         int lo = 0, hi = 0;
         if (first < N) {
             const int last = min(first + kTileRows - 1, N - 1);
-            hi = kCausal ? min(nkv_all, last / kTileRows + 1) : nkv_all;
+            hi = kCausal ? (last + off >= 0 ? min(nkv_all, (last + off) / kTileRows + 1) : 0)
+                         : nkv_all;
             if (W > 0) {
-                lo = max(0, first - W + 1) / kTileRows;
-                if (!kCausal) hi = min(nkv_all, (last + W - 1) / kTileRows + 1);
+                lo = max(0, first + off - W + 1) / kTileRows;
+                if (!kCausal) hi = max(0, min(nkv_all, (last + off + W - 1) / kTileRows + 1));
             }
             lo = min(lo, hi);
         }
@@ -214,8 +219,8 @@ __global__ void __launch_bounds__(320, 1)
                     }
                     if (kTF32 && which == 1) {
                         store_v_transposed<D>(static_cast<const float*>(p.V) +
-                                                  static_cast<size_t>(bh) * N * D,
-                                              sKV + slot * C::TILE, j * kTileRows, N, lane);
+                                                  static_cast<size_t>(bh) * Nk * D,
+                                              sKV + slot * C::TILE, j * kTileRows, Nk, lane);
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&full[slot]);
@@ -359,16 +364,16 @@ __global__ void __launch_bounds__(320, 1)
             tc_fence_after();
             const int k0 = j * kTileRows;
             const int tile_last_row = tile_first_row + kTileRows - 1;
-            const bool wmask = W > 0 && (k0 < tile_last_row - W + 1 ||
-                                         (!kCausal && k0 + kTileRows - 1 > tile_first_row + W - 1));
+            const bool wmask = W > 0 && (k0 < tile_last_row + off - W + 1 ||
+                                         (!kCausal && k0 + kTileRows - 1 > tile_first_row + off + W - 1));
             const bool tile_mask = (k0 + kTileRows > L) ||
-                                   (kCausal && k0 + kTileRows - 1 > tile_first_row) || wmask;
+                                   (kCausal && k0 + kTileRows - 1 > tile_first_row + off) || wmask;
             // columns >= lim and < lo of this row are masked (only on masked tiles)
-            int lim = tile_mask ? (kCausal ? min(L, row + 1) : L) - k0 : kTileRows;
+            int lim = tile_mask ? (kCausal ? min(L, row + off + 1) : L) - k0 : kTileRows;
             int lo = 0;
             if (wmask) {
-                lo = row - W + 1 - k0;
-                if (!kCausal) lim = min(lim, row + W - k0);
+                lo = row + off - W + 1 - k0;
+                if (!kCausal) lim = min(lim, row + off + W - k0);
             }
 
             // ---- pass 1: row max (S read from TMEM, eight independent chains) ----

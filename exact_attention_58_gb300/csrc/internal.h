@@ -19,7 +19,8 @@ struct FwdParams {
     float* LSE;
     const int32_t* key_lens;
     int* dev_status;
-    int B, H, N;
+    int B, H, N;              // N: query rows
+    int Nk;                   // keys (N_k != N: cross-attention)
     int nqb;                  // query blocks of kFwdRowsPerCta rows
     float scale_log2;         // scale * log2(e)
     float out_scale;          // 1 / (1 - dropout_p)
@@ -36,7 +37,8 @@ struct BwdParams {
     float* dq_acc;            // [B*H][Npad][d] fp32
     const float* lse2;        // [B*H][Npad] LSE * log2(e); +inf marks "no contribution"
     const float* Drow;        // [B*H][Npad] dO . O
-    int B, H, N, Npad;
+    int B, H, N, Npad;        // N: query rows, Npad: N rounded up to 128
+    int Nk;                   // keys
     int nkb;                  // key blocks of kTileRows rows
     float scale_log2;
     float scale;              // applied to dK

@@ -53,19 +53,21 @@ attn_status scratch_on_current_device(void** out) {
 
 extern "C" attn_status attn_bwd_noalloc(const void* Q, const void* K, const void* V,
                                         const void* O, const void* dO, const float* LSE,
-                                        void* dQ, void* dK, void* dV, int B, int H, int N, int d,
-                                        attn_dtype dtype, float scale, int causal, int window,
+                                        void* dQ, void* dK, void* dV, int B, int H, int N,
+                                        int Nk, int d, attn_dtype dtype, float scale, int causal,
+                                        int window,
                                         const int32_t* key_lens, float dropout_p, uint64_t seed,
                                         int* dev_status, void* stream) {
     const size_t need = attn_bwd_workspace_size(B, H, N, d);
     const bool null_arg = !Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV;
     if (need == 0 || null_arg)   // rejected arguments: attn_bwd says why, before any CUDA call
-        return attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, dtype, scale, causal, window,
-                        key_lens, dropout_p, seed, nullptr, 0, dev_status, stream);
+        return attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, Nk, d, dtype, scale, causal,
+                        window, key_lens, dropout_p, seed, nullptr, 0, dev_status, stream);
     if (need > gbattn::kNoAllocScratchBytes) return ATTN_ERR_WORKSPACE;
     void* scratch = nullptr;
     const attn_status st = gbattn::scratch_on_current_device(&scratch);
     if (st != ATTN_OK) return st;
-    return attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, dtype, scale, causal, window, key_lens,
-                    dropout_p, seed, scratch, gbattn::kNoAllocScratchBytes, dev_status, stream);
+    return attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, Nk, d, dtype, scale, causal, window,
+                    key_lens, dropout_p, seed, scratch, gbattn::kNoAllocScratchBytes, dev_status,
+                    stream);
 }

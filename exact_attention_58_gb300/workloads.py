@@ -7,8 +7,9 @@ The five workloads stand in for the shapes the pages measure on (GPT-2 small,
 BERT-large, long sequences) with iid Gaussian data; no dataset or trained
 weight is used.  Recipe for workload c (1-based):
   * a CPU ``torch.Generator`` seeded with 1000 + c;
-  * float32 N(0, sigma^2) drawn in the order Q, K, V, dO (each [B, H, N, d]),
-    then the per-sequence key lengths (uniform integers in [lo, hi]);
+  * float32 N(0, sigma^2) drawn in the order Q, K, V, dO (Q and dO [B, H, N, d],
+    K and V [B, H, Nk, d] with Nk = N unless a key length is given), then the
+    per-sequence key lengths (uniform integers in [lo, hi], at most Nk);
   * Q, K, V, dO cast to the workload dtype (bf16 rounds to nearest even);
   * the dropout seed is 0x5EED0000 + c.
 """
@@ -85,29 +86,33 @@ class Inputs:
 def make_inputs(B: int, H: int, N: int, d: int, *, dtype=torch.bfloat16, sigma: float = 1.0,
                 gen_seed: int = 0, causal: bool = False, key_len_range=None,
                 dropout_p: float = 0.0, dropout_seed_value: int = 0, with_do: bool = True,
-                scale: Optional[float] = None) -> Inputs:
-    """Draw one seeded input set on the CPU (see the module docstring for the order)."""
+                scale: Optional[float] = None, Nk: Optional[int] = None) -> Inputs:
+    """Draw one seeded input set on the CPU (see the module docstring for the
+    order).  ``Nk`` (default N) keys: cross-attention when it differs from N."""
     g = torch.Generator(device="cpu")
     g.manual_seed(int(gen_seed))
     shape = (B, H, N, d)
+    Nk = N if Nk is None else int(Nk)
+    kshape = (B, H, Nk, d)
     q = (torch.randn(shape, generator=g, dtype=torch.float32) * sigma).to(dtype)
-    k = (torch.randn(shape, generator=g, dtype=torch.float32) * sigma).to(dtype)
-    v = (torch.randn(shape, generator=g, dtype=torch.float32) * sigma).to(dtype)
+    k = (torch.randn(kshape, generator=g, dtype=torch.float32) * sigma).to(dtype)
+    v = (torch.randn(kshape, generator=g, dtype=torch.float32) * sigma).to(dtype)
     do = (torch.randn(shape, generator=g, dtype=torch.float32)).to(dtype) if with_do else None
     kl = None
     if key_len_range is not None:
         lo, hi = key_len_range
         kl = torch.randint(int(lo), int(hi) + 1, (B,), generator=g, dtype=torch.int64)
-        kl = kl.clamp(max=N).to(torch.int32)
+        kl = kl.clamp(max=Nk).to(torch.int32)
     return Inputs(q, k, v, do, kl, (1.0 / math.sqrt(d)) if scale is None else float(scale),
                   causal, float(dropout_p), int(dropout_seed_value))
 
 
 def make_workload_inputs(index: int, B: Optional[int] = None, H: Optional[int] = None,
-                         N: Optional[int] = None) -> Inputs:
-    """Inputs of workload ``index`` (1-based), optionally with B/H/N cut down."""
+                         N: Optional[int] = None, Nk: Optional[int] = None) -> Inputs:
+    """Inputs of workload ``index`` (1-based), optionally with B/H/N cut down
+    or with ``Nk`` keys (cross-attention) instead of N."""
     w = workload(index)
     return make_inputs(B or w.B, H or w.H, N or w.N, w.d, dtype=w.torch_dtype, sigma=w.sigma,
                        gen_seed=1000 + index, causal=w.causal, key_len_range=w.key_len_range,
                        dropout_p=w.dropout_p, dropout_seed_value=dropout_seed(index),
-                       with_do=w.backward)
+                       with_do=w.backward, Nk=Nk)

@@ -18,10 +18,12 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  Layout     Q, K, V, O, dO, dQ, dK, dV are contiguous [B, H, N, d] arrays,
- *             d innermost (row-major), one element type for all of them.
- *             LSE is a contiguous float [B, H, N] array.  key_lens is an
- *             int32 [B] array.  Every pointer is a DEVICE pointer.
+ *  Layout     Q, O, dO, dQ are contiguous [B, H, N, d] arrays and K, V, dK,
+ *             dV contiguous [B, H, Nk, d] arrays, d innermost (row-major), one
+ *             element type for all of them.  N is the number of query rows and
+ *             Nk the number of keys (Nk = N for self-attention).  LSE is a
+ *             contiguous float [B, H, N] array.  key_lens is an int32 [B]
+ *             array.  Every pointer is a DEVICE pointer.
  *  Alignment  Every tensor pointer must be 16-byte aligned
  *             (ATTN_ERR_MISALIGNED otherwise).
  *  Types      ATTN_DTYPE_BF16: bf16 storage, bf16 x bf16 products with fp32
@@ -29,18 +31,21 @@
  *             storage and f16 x f16 products (P and dS are rounded to f16).
  *             ATTN_DTYPE_FP32: fp32 storage, TF32 products with fp32
  *             accumulation (forward only, d = 64).
- *  Shapes     d in {64, 128}; B, H, N >= 1; B*H*N*d < 2^31 elements per
- *             tensor.  Anything else returns ATTN_ERR_UNSUPPORTED or
+ *  Shapes     d in {64, 128}; B, H, N, Nk >= 1; B*H*N*d and B*H*Nk*d
+ *             < 2^31 elements per tensor.  Anything else returns ATTN_ERR_UNSUPPORTED or
  *             ATTN_ERR_INVALID_ARG: the library never falls back to another
  *             implementation.
- *  Mask       key j of sequence b is attended iff j < key_lens[b] (all N keys
- *             when key_lens is NULL), when causal != 0, j <= i, and, when
- *             window > 0 (sliding-window attention), i - j < window and, unless
- *             causal, j - i < window; window <= 0 means no window.  Key blocks
- *             outside the window are skipped, not computed and masked.  A query
- *             row with no valid key gets O = 0 and LSE = -inf (and zero
- *             gradients).  key_lens values outside [0, N] are clamped on the
- *             device and reported as ATTN_ERR_INVALID_ARG through dev_status.
+ *  Mask       query i stands at key position p = i + Nk - N: with N != Nk the
+ *             queries are the last N positions of the key sequence (p = i
+ *             for self-attention).  Key j of sequence b is attended by query i
+ *             iff j < key_lens[b] (all Nk keys when key_lens is NULL), when
+ *             causal != 0, j <= p, and, when window > 0 (sliding-window
+ *             attention), p - j < window and, unless causal, j - p < window;
+ *             window <= 0 means no window.  Key blocks outside the mask are
+ *             skipped, not computed and masked.  A query row with no valid key
+ *             gets O = 0 and LSE = -inf (and zero gradients).  key_lens values
+ *             outside [0, Nk] are clamped on the device and reported as
+ *             ATTN_ERR_INVALID_ARG through dev_status.
  *  Scale      scale must be finite and > 0 (1/sqrt(d) is the usual choice).
  *  Dropout    0 <= dropout_p < 1.  Kept probabilities are multiplied by
  *             1/(1 - dropout_p); the softmax denominator and LSE use the
@@ -91,7 +96,8 @@ typedef enum {
 
 /*
  * Forward pass.
- *   Q, K, V   in   [B, H, N, d]
+ *   Q         in   [B, H, N, d]
+ *   K, V      in   [B, H, Nk, d]
  *   O         out  [B, H, N, d]  (same dtype as Q)
  *   LSE       out  [B, H, N] float: natural log of the sum over valid keys of
  *                  exp(scale * q_i . k_j) (-inf for a row with no valid key)
@@ -99,30 +105,32 @@ typedef enum {
  * products) with d = 64.
  */
 attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                     int B, int H, int N, int d, attn_dtype dtype, float scale, int causal, int window,
-                     const int32_t* key_lens, float dropout_p, uint64_t seed,
-                     int* dev_status, void* stream);
+                     int B, int H, int N, int Nk, int d, attn_dtype dtype, float scale,
+                     int causal, int window, const int32_t* key_lens, float dropout_p,
+                     uint64_t seed, int* dev_status, void* stream);
 
 /*
  * Bytes of device workspace attn_bwd needs: per head, the row terms
  * D_i = dO_i . O_i and the log-sum-exp in base 2 (two floats per row) and an
- * fp32 accumulator for dQ, with N rounded up to a multiple of 128.
- * Returns 0 for arguments attn_bwd would reject.
+ * fp32 accumulator for dQ, with N (query rows) rounded up to a multiple of
+ * 128.  It does not depend on Nk.  Returns 0 for arguments attn_bwd would
+ * reject.
  */
 size_t attn_bwd_workspace_size(int B, int H, int N, int d);
 
 /*
  * Backward pass: given the forward's inputs, its O and LSE and the incoming
- * gradient dO, writes dQ, dK, dV (same dtype and layout as Q).  bf16 only,
- * d in {64, 128}.  workspace must hold attn_bwd_workspace_size(B, H, N, d)
+ * gradient dO, writes dQ ([B, H, N, d]) and dK, dV ([B, H, Nk, d]), in the
+ * dtype of Q.  bf16 or fp16, d in {64, 128}.  workspace must hold attn_bwd_workspace_size(B, H, N, d)
  * bytes (16-byte aligned); its contents on entry do not matter.  Enqueues
  * three launches: attn_bwd_preprocess, attn_bwd_main, attn_bwd_dq_convert.
  */
 attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
                      const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
-                     int B, int H, int N, int d, attn_dtype dtype, float scale, int causal, int window,
-                     const int32_t* key_lens, float dropout_p, uint64_t seed,
-                     void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
+                     int B, int H, int N, int Nk, int d, attn_dtype dtype, float scale,
+                     int causal, int window, const int32_t* key_lens, float dropout_p,
+                     uint64_t seed, void* workspace, size_t workspace_bytes, int* dev_status,
+                     void* stream);
 
 /*
  * The three stages of attn_bwd, exported so that a caller can enqueue (and
@@ -138,10 +146,10 @@ attn_status attn_bwd_preprocess(const void* O, const void* dO, const float* LSE,
                                 int B, int H, int N, int d, attn_dtype dtype,
                                 void* workspace, size_t workspace_bytes, void* stream);
 attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO,
-                          void* dK, void* dV, int B, int H, int N, int d, attn_dtype dtype,
-                          float scale, int causal, int window, const int32_t* key_lens, float dropout_p,
-                          uint64_t seed, void* workspace, size_t workspace_bytes,
-                          int* dev_status, void* stream);
+                          void* dK, void* dV, int B, int H, int N, int Nk, int d,
+                          attn_dtype dtype, float scale, int causal, int window,
+                          const int32_t* key_lens, float dropout_p, uint64_t seed,
+                          void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
 attn_status attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, attn_dtype dtype,
                                 float scale, const void* workspace, size_t workspace_bytes,
                                 void* stream);
@@ -167,7 +175,7 @@ attn_status attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, attn_dtype
  */
 attn_status attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
                              const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
-                             int B, int H, int N, int d, attn_dtype dtype, float scale,
+                             int B, int H, int N, int Nk, int d, attn_dtype dtype, float scale,
                              int causal, int window, const int32_t* key_lens, float dropout_p,
                              uint64_t seed, int* dev_status, void* stream);
 

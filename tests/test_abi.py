@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"libgbattn.so does not export {name}"
     # and nothing in the shared object is a C++-only stand-in
-    assert lib.attn_version() == 100
+    assert lib.attn_version() == 200
 
 
 def test_status_strings(lib):
@@ -55,8 +55,9 @@ def _fwd(lib, **kw):
              scale=0.125, causal=0, window=0, key_lens=None, p=0.0, seed=0, dev_status=None,
              stream=None)
     a.update(kw)
+    a.setdefault("Nk", a["N"])
     return lib.attn_fwd(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["H"], a["N"],
-                        a["d"], a["dtype"], a["scale"], a["causal"], a["window"], a["key_lens"],
+                        a["Nk"], a["d"], a["dtype"], a["scale"], a["causal"], a["window"], a["key_lens"],
                         a["p"], a["seed"], a["dev_status"], a["stream"])
 
 
@@ -64,6 +65,8 @@ def _fwd(lib, **kw):
     (dict(Q=None), 1),
     (dict(LSE=None), 1),
     (dict(N=0), 1),
+    (dict(Nk=0), 1),
+    (dict(N=128, Nk=-5), 1),
     (dict(B=-1), 1),
     (dict(d=96), 2),
     (dict(d=256), 2),
@@ -79,6 +82,7 @@ def _fwd(lib, **kw):
     (dict(K=FAKE + 8), 3),
     (dict(O=FAKE + 2), 3),
     (dict(B=65536, H=65536), 2),
+    (dict(B=64, H=64, N=128, Nk=1 << 20), 2),
 ])
 def test_fwd_validation(lib, kw, expected):
     assert _fwd(lib, **kw) == expected
@@ -88,7 +92,8 @@ def _bwd(lib, **kw):
     a = dict(B=1, H=1, N=128, d=64, dtype=0, scale=0.125, p=0.0, ws=FAKE, ws_bytes=1 << 20,
              ptrs=[FAKE] * 9)
     a.update(kw)
-    return lib.attn_bwd(*a["ptrs"], a["B"], a["H"], a["N"], a["d"], a["dtype"], a["scale"], 0,
+    a.setdefault("Nk", a["N"])
+    return lib.attn_bwd(*a["ptrs"], a["B"], a["H"], a["N"], a["Nk"], a["d"], a["dtype"], a["scale"], 0,
                         0, None, a["p"], 0, a["ws"], a["ws_bytes"], None, None)
 
 
@@ -103,6 +108,8 @@ def _bwd(lib, **kw):
     (dict(ws=FAKE + 4), 3),
     (dict(ptrs=[FAKE] * 5 + [FAKE + 4] + [FAKE] * 3), 3),
     (dict(p=1.5), 1),
+    (dict(Nk=0), 1),
+    (dict(B=64, H=64, Nk=1 << 20), 2),
 ])
 def test_bwd_validation(lib, kw, expected):
     assert _bwd(lib, **kw) == expected

@@ -22,10 +22,11 @@ pytestmark = pytest.mark.gpu
 def _call_noalloc(lib, q, k, v, o, do, lse, dq, dk, dv, inp, status):
     """Straight through the C ABI: no workspace argument at all."""
     B, H, N, d = q.shape
+    Nk = k.shape[2]
     p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
     kl = None if inp.key_lens is None else ctypes.c_void_p(inp.key_lens.cuda().data_ptr())
     return lib.attn_bwd_noalloc(p(q), p(k), p(v), p(o), p(do), p(lse), p(dq), p(dk), p(dv),
-                                B, H, N, d, 0, inp.scale, int(inp.causal), 0, kl, inp.dropout_p,
+                                B, H, N, Nk, d, 0, inp.scale, int(inp.causal), 0, kl, inp.dropout_p,
                                 inp.seed, p(status),
                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
@@ -57,6 +58,6 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     lib = ea.library()
     fake = ctypes.c_void_p(0x10000)
     # 64 heads x 4096 rows x (2 + 128) floats = 136 MB > 32 MiB
-    st = lib.attn_bwd_noalloc(*([fake] * 9), 4, 16, 4096, 128, 0, 0.088, 1, 0, None, 0.0, 0,
+    st = lib.attn_bwd_noalloc(*([fake] * 9), 4, 16, 4096, 4096, 128, 0, 0.088, 1, 0, None, 0.0, 0,
                               None, None)
     assert st == 4   # ATTN_ERR_WORKSPACE, before anything is enqueued
