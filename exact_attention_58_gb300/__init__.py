@@ -28,7 +28,8 @@ from . import _build
 
 __all__ = [
     "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
-    "attn_bwd_main", "attn_bwd_dq_convert", "attn_bwd_noalloc", "attn_status_string", "attn_version", "library",
+    "attn_bwd_main", "attn_bwd_dq_convert", "attn_bwd_noalloc", "attn_fwd_varlen",
+    "attn_bwd_varlen", "attn_status_string", "attn_version", "library",
     "LIB_PATH", "STATUS",
 ]
 
@@ -79,8 +80,12 @@ def library():
             lib.attn_bwd_main.argtypes = [vp] * 6 + [ip] * 6 + [f, ip, ip, vp, f, u64, vp, sz, vp,
                                                               vp]
             lib.attn_bwd_dq_convert.argtypes = [vp, ip, ip, ip, ip, ip, f, vp, sz, vp]
+            lib.attn_fwd_varlen.argtypes = [vp] * 7 + [ip] * 8 + [f, ip, ip, f, u64, vp, vp]
+            lib.attn_bwd_varlen.argtypes = ([vp] * 11 + [ip] * 8 +
+                                            [f, ip, ip, f, u64, vp, sz, vp, vp])
             for fn in ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
-                       "attn_bwd_dq_convert", "attn_bwd_noalloc"):
+                       "attn_bwd_dq_convert", "attn_bwd_noalloc", "attn_fwd_varlen",
+                       "attn_bwd_varlen"):
                 getattr(lib, fn).restype = ctypes.c_int
             lib.attn_status_string.argtypes = [ctypes.c_int]
             lib.attn_status_string.restype = ctypes.c_char_p
@@ -288,3 +293,92 @@ def attn_bwd_dq_convert(dq, workspace, *, scale=None, stream=None):
                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
                                        _stream(stream))
     _raise(st, "attn_bwd_dq_convert")
+
+
+# ---------------------------------------------------------------------------
+# packed variable-length sequences
+# ---------------------------------------------------------------------------
+def _packed(name: str, t: torch.Tensor, H: int, d: int, ref: torch.Tensor):
+    if (t.dim() != 3 or t.shape[1] != H or t.shape[2] != d or t.dtype != ref.dtype
+            or t.device != ref.device):
+        raise ValueError(f"{name} must be [total, H, d] with q's H, d, dtype and device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return int(t.shape[0])
+
+
+def _cu(name: str, cu, q: torch.Tensor) -> int:
+    if (not isinstance(cu, torch.Tensor) or cu.dtype != torch.int32 or cu.device != q.device
+            or cu.dim() != 1 or cu.numel() < 2 or not cu.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous int32 [B + 1] tensor on q's device")
+    return int(cu.numel()) - 1
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int, *,
+                    causal: bool = False, window: int = 0, dropout_p: float = 0.0, seed: int = 0,
+                    scale: Optional[float] = None, out=None, lse=None, dev_status=None,
+                    stream=None):
+    """Attention over packed sequences: q [total_q, H, d], k, v [total_k, H, d],
+    sequence b at rows [cu[b], cu[b+1]).  Returns O [total_q, H, d] and LSE
+    [H, total_q]; see include/gbattn.h."""
+    if q.dim() != 3:
+        raise ValueError("expected q as [total_q, H, d]")
+    total_q, H, d = (int(x) for x in q.shape)
+    _packed("q", q, H, d, q)
+    total_k = _packed("k", k, H, d, q)
+    if _packed("v", v, H, d, q) != total_k:
+        raise ValueError("v must match k")
+    B = _cu("cu_seqlens_q", cu_seqlens_q, q)
+    if _cu("cu_seqlens_k", cu_seqlens_k, q) != B:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _check_like("out", out, q)
+    if lse is None:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    st = library().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                   _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, H, total_q, total_k,
+                                   int(max_seqlen_q), int(max_seqlen_k), d, _dtype_code(q),
+                                   float(scale), int(bool(causal)), int(window), float(dropout_p),
+                                   int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(dev_status),
+                                   _stream(stream))
+    _raise(st, "attn_fwd_varlen")
+    return out, lse
+
+
+def attn_bwd_varlen(q, k, v, o, do, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                    max_seqlen_k: int, *, causal: bool = False, window: int = 0,
+                    dropout_p: float = 0.0, seed: int = 0, scale: Optional[float] = None,
+                    dq=None, dk=None, dv=None, workspace=None, dev_status=None, stream=None):
+    """dQ, dK, dV of attn_fwd_varlen (same packed layouts)."""
+    if q.dim() != 3:
+        raise ValueError("expected q as [total_q, H, d]")
+    total_q, H, d = (int(x) for x in q.shape)
+    total_k = _packed("k", k, H, d, q)
+    if _packed("v", v, H, d, q) != total_k:
+        raise ValueError("v must match k")
+    for name, t in (("o", o), ("do", do)):
+        _check_like(name, t, q)
+    B = _cu("cu_seqlens_q", cu_seqlens_q, q)
+    if _cu("cu_seqlens_k", cu_seqlens_k, q) != B:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(k) if dv is None else dv
+    _check_like("dq", dq, q)
+    _check_like("dk", dk, k)
+    _check_like("dv", dv, k)
+    ws, ws_bytes = _workspace(B, H, int(max_seqlen_q), d, workspace, q.device)
+    st = library().attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q),
+                                   _ptr(cu_seqlens_k), B, H, total_q, total_k, int(max_seqlen_q),
+                                   int(max_seqlen_k), d, _dtype_code(q), float(scale),
+                                   int(bool(causal)), int(window), float(dropout_p),
+                                   int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(ws), ws_bytes,
+                                   _ptr(dev_status), _stream(stream))
+    _raise(st, "attn_bwd_varlen")
+    return dq, dk, dv

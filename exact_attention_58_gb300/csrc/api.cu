@@ -89,28 +89,195 @@ attn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_
 
 }  // namespace
 
-bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int BH, int N, int d) {
-    const bool fp32 = dtype == ATTN_DTYPE_FP32;
+namespace {
+
+bool encode_3d(CUtensorMap* map, const void* ptr, attn_dtype dtype, const cuuint64_t dims[3],
+               const cuuint64_t strides[2], const cuuint32_t box[3]) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (enc == nullptr) return false;
-    const cuuint64_t es = fp32 ? 4 : 2;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType ty =
+        dtype == ATTN_DTYPE_FP32
+            ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+            : (dtype == ATTN_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    const CUresult r = enc(map, ty, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int BH, int N, int d) {
+    const cuuint64_t es = dtype == ATTN_DTYPE_FP32 ? 4 : 2;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es,
                                    static_cast<cuuint64_t>(N) * d * es};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(kTileRows), 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r =
-        enc(map,
-            fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                 : (dtype == ATTN_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16),
-            3,
-            const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode_3d(map, ptr, dtype, dims, strides, box);
 }
 
+bool make_tmap_thd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int T, int H, int d) {
+    const cuuint64_t es = dtype == ATTN_DTYPE_FP32 ? 4 : 2;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(T)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es,
+                                   static_cast<cuuint64_t>(H) * d * es};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 1, static_cast<cuuint32_t>(kTileRows)};
+    return encode_3d(map, ptr, dtype, dims, strides, box);
+}
+
+namespace {
+
+// Map over one activation tensor: [B*H][N][d] when dense, [T][H][d] when packed.
+bool make_tmap(CUtensorMap* map, const void* ptr, attn_dtype dtype, int B, const SeqLayout& l,
+               int d) {
+    return l.cu ? make_tmap_thd(map, ptr, dtype, l.total, l.H, d)
+                : make_tmap_bhnd(map, ptr, dtype, B * l.H, l.N, d);
+}
+
+// Checks of the packed-sequence entry points, on top of those of the dense
+// ones with N = max_seqlen_q and Nk = max_seqlen_k.
+attn_status check_varlen(const int32_t* cu_q, const int32_t* cu_k, int B, int H, int total_q,
+                         int total_k, int max_q, int max_k, int d, attn_dtype dtype,
+                         bool backward) {
+    if (cu_q == nullptr || cu_k == nullptr) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(cu_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_k) & 3u))
+        return ATTN_ERR_MISALIGNED;
+    if (total_q < 1 || total_k < 1 || max_q < 1 || max_k < 1) return ATTN_ERR_INVALID_ARG;
+    attn_status st = check_shape(B, H, max_q, d, dtype, backward);
+    if (st != ATTN_OK) return st;
+    if ((st = check_keys(B, H, max_k, d)) != ATTN_OK) return st;
+    if (dtype == ATTN_DTYPE_FP32) return ATTN_ERR_UNSUPPORTED;   // packed: 16-bit types only
+    if (static_cast<long long>(total_q) * H * d >= (1LL << 31) ||
+        static_cast<long long>(total_k) * H * d >= (1LL << 31))
+        return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+// The forward for validated shapes.
+attn_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                     const SeqLayout& lq, const SeqLayout& lk, int d, attn_dtype dtype,
+                     float scale, int causal, int window, const int32_t* key_lens,
+                     float dropout_p, uint64_t seed, int* dev_status, void* stream) {
+    attn_status st = check_math(scale, dropout_p);
+    if (st != ATTN_OK) return st;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+        return ATTN_ERR_MISALIGNED;
+    CUtensorMap tq, tk, tv;
+    if (!make_tmap(&tq, Q, dtype, B, lq, d) || !make_tmap(&tk, K, dtype, B, lk, d) ||
+        !make_tmap(&tv, V, dtype, B, lk, d))
+        return ATTN_ERR_CUDA;
+    FwdParams p{};
+    p.V = V;
+    p.O = O;
+    p.LSE = LSE;
+    p.key_lens = key_lens;
+    p.dev_status = dev_status;
+    p.B = B;
+    p.H = lq.H;
+    p.N = lq.N;
+    p.Nk = lk.N;
+    p.nqb = (lq.N + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.out_scale = 1.0f / (1.0f - dropout_p);
+    p.drop_threshold = drop_threshold(dropout_p);
+    p.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFu);
+    p.seed_hi = static_cast<uint32_t>(seed >> 32);
+    p.window = window > 0 ? window : 0;
+    p.lq = lq;
+    p.lk = lk;
+    return from_cuda(launch_fwd(tq, tk, tv, p, d, dtype, causal != 0, dropout_p > 0.f,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+attn_status pre_impl(const void* O, const void* dO, const float* LSE, int B, const SeqLayout& lq,
+                     int d, attn_dtype dtype, void* workspace, void* stream) {
+    if (!aligned16(O) || !aligned16(dO) || !aligned16(LSE)) return ATTN_ERR_MISALIGNED;
+    const Workspace w = carve(workspace, B, lq.H, lq.N);
+    return from_cuda(launch_bwd_pre(O, dO, LSE, w.lse2, w.Drow, w.dq_acc, B * lq.H, lq,
+                                    npad_of(lq.N), d, dtype == ATTN_DTYPE_FP16,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+attn_status main_impl(const void* Q, const void* K, const void* V, const void* dO, void* dK,
+                      void* dV, int B, const SeqLayout& lq, const SeqLayout& lk, int d,
+                      attn_dtype dtype, float scale, int causal, int window,
+                      const int32_t* key_lens, float dropout_p, uint64_t seed, void* workspace,
+                      int* dev_status, void* stream) {
+    attn_status st = check_math(scale, dropout_p);
+    if (st != ATTN_OK) return st;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(dK) ||
+        !aligned16(dV))
+        return ATTN_ERR_MISALIGNED;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+    if (!make_tmap(&tq, Q, dtype, B, lq, d) || !make_tmap(&tk, K, dtype, B, lk, d) ||
+        !make_tmap(&tv, V, dtype, B, lk, d) || !make_tmap(&tdo, dO, dtype, B, lq, d) ||
+        !make_tmap(&tdk, dK, dtype, B, lk, d) || !make_tmap(&tdv, dV, dtype, B, lk, d))
+        return ATTN_ERR_CUDA;
+    const Workspace w = carve(workspace, B, lq.H, lq.N);
+    BwdParams p{};
+    p.dK = dK;
+    p.dV = dV;
+    p.key_lens = key_lens;
+    p.dev_status = dev_status;
+    p.dq_acc = w.dq_acc;
+    p.lse2 = w.lse2;
+    p.Drow = w.Drow;
+    p.B = B;
+    p.H = lq.H;
+    p.N = lq.N;
+    p.Nk = lk.N;
+    p.Npad = npad_of(lq.N);
+    p.nkb = (lk.N + kTileRows - 1) / kTileRows;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.scale = scale;
+    p.drop_scale = 1.0f / (1.0f - dropout_p);
+    p.drop_threshold = drop_threshold(dropout_p);
+    p.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFu);
+    p.seed_hi = static_cast<uint32_t>(seed >> 32);
+    p.window = window > 0 ? window : 0;
+    p.lq = lq;
+    p.lk = lk;
+    return from_cuda(launch_bwd_main(tq, tk, tv, tdo, tdk, tdv, p, d, dtype == ATTN_DTYPE_FP16,
+                                     causal != 0, dropout_p > 0.f,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+attn_status convert_impl(void* dQ, int B, const SeqLayout& lq, int d, attn_dtype dtype,
+                         float scale, const void* workspace, void* stream) {
+    if (!aligned16(dQ)) return ATTN_ERR_MISALIGNED;
+    const Workspace w = carve(const_cast<void*>(workspace), B, lq.H, lq.N);
+    return from_cuda(launch_bwd_dq_convert(dQ, w.dq_acc, B * lq.H, lq, npad_of(lq.N), d,
+                                           dtype == ATTN_DTYPE_FP16, scale,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+// The whole backward for validated shapes: every argument is checked before
+// the first launch so that errors leave the outputs untouched.
+attn_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                     const float* LSE, void* dQ, void* dK, void* dV, int B, const SeqLayout& lq,
+                     const SeqLayout& lk, int d, attn_dtype dtype, float scale, int causal,
+                     int window, const int32_t* key_lens, float dropout_p, uint64_t seed,
+                     void* workspace, size_t workspace_bytes, int* dev_status, void* stream) {
+    attn_status st = check_math(scale, dropout_p);
+    if (st != ATTN_OK) return st;
+    if ((st = check_workspace(workspace, workspace_bytes, B, lq.H, lq.N, d)) != ATTN_OK) return st;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) ||
+        !aligned16(LSE) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
+        return ATTN_ERR_MISALIGNED;
+    if ((st = pre_impl(O, dO, LSE, B, lq, d, dtype, workspace, stream)) != ATTN_OK) return st;
+    if ((st = main_impl(Q, K, V, dO, dK, dV, B, lq, lk, d, dtype, scale, causal, window, key_lens,
+                        dropout_p, seed, workspace, dev_status, stream)) != ATTN_OK)
+        return st;
+    return convert_impl(dQ, B, lq, d, dtype, scale, workspace, stream);
+}
+
+SeqLayout dense(int H, int N) { return SeqLayout{nullptr, H, N, 0}; }
+
+}  // namespace
 }  // namespace gbattn
 
 using namespace gbattn;
@@ -125,32 +292,22 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
     attn_status st = check_shape(B, H, N, d, dtype, false);
     if (st != ATTN_OK) return st;
     if ((st = check_keys(B, H, Nk, d)) != ATTN_OK) return st;
-    if ((st = check_math(scale, dropout_p)) != ATTN_OK) return st;
-    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
-        return ATTN_ERR_MISALIGNED;
-    CUtensorMap tq, tk, tv;
-    if (!make_tmap_bhnd(&tq, Q, dtype, B * H, N, d) || !make_tmap_bhnd(&tk, K, dtype, B * H, Nk, d) ||
-        !make_tmap_bhnd(&tv, V, dtype, B * H, Nk, d))
-        return ATTN_ERR_CUDA;
-    FwdParams p{};
-    p.V = V;
-    p.O = O;
-    p.LSE = LSE;
-    p.key_lens = key_lens;
-    p.dev_status = dev_status;
-    p.B = B;
-    p.H = H;
-    p.N = N;
-    p.Nk = Nk;
-    p.nqb = (N + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.out_scale = 1.0f / (1.0f - dropout_p);
-    p.drop_threshold = drop_threshold(dropout_p);
-    p.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFu);
-    p.seed_hi = static_cast<uint32_t>(seed >> 32);
-    p.window = window > 0 ? window : 0;
-    return from_cuda(launch_fwd(tq, tk, tv, p, d, dtype, causal != 0, dropout_p > 0.f,
-                                static_cast<cudaStream_t>(stream)));
+    return fwd_impl(Q, K, V, O, LSE, B, dense(H, N), dense(H, Nk), d, dtype, scale, causal, window,
+                    key_lens, dropout_p, seed, dev_status, stream);
+}
+
+attn_status attn_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int B, int H,
+                            int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                            attn_dtype dtype, float scale, int causal, int window,
+                            float dropout_p, uint64_t seed, int* dev_status, void* stream) {
+    if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
+    const attn_status st = check_varlen(cu_seqlens_q, cu_seqlens_k, B, H, total_q, total_k,
+                                        max_seqlen_q, max_seqlen_k, d, dtype, false);
+    if (st != ATTN_OK) return st;
+    return fwd_impl(Q, K, V, O, LSE, B, SeqLayout{cu_seqlens_q, H, max_seqlen_q, total_q},
+                    SeqLayout{cu_seqlens_k, H, max_seqlen_k, total_k}, d, dtype, scale, causal,
+                    window, nullptr, dropout_p, seed, dev_status, stream);
 }
 
 size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
@@ -165,10 +322,7 @@ attn_status attn_bwd_preprocess(const void* O, const void* dO, const float* LSE,
     attn_status st = check_shape(B, H, N, d, dtype, true);
     if (st != ATTN_OK) return st;
     if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != ATTN_OK) return st;
-    if (!aligned16(O) || !aligned16(dO) || !aligned16(LSE)) return ATTN_ERR_MISALIGNED;
-    const Workspace w = carve(workspace, B, H, N);
-    return from_cuda(launch_bwd_pre(O, dO, LSE, w.lse2, w.Drow, w.dq_acc, B * H, N, npad_of(N),
-                                    d, dtype == ATTN_DTYPE_FP16, static_cast<cudaStream_t>(stream)));
+    return pre_impl(O, dO, LSE, B, dense(H, N), d, dtype, workspace, stream);
 }
 
 attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dK,
@@ -180,41 +334,9 @@ attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const voi
     attn_status st = check_shape(B, H, N, d, dtype, true);
     if (st != ATTN_OK) return st;
     if ((st = check_keys(B, H, Nk, d)) != ATTN_OK) return st;
-    if ((st = check_math(scale, dropout_p)) != ATTN_OK) return st;
     if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != ATTN_OK) return st;
-    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(dK) ||
-        !aligned16(dV))
-        return ATTN_ERR_MISALIGNED;
-    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-    if (!make_tmap_bhnd(&tq, Q, dtype, B * H, N, d) || !make_tmap_bhnd(&tk, K, dtype, B * H, Nk, d) ||
-        !make_tmap_bhnd(&tv, V, dtype, B * H, Nk, d) || !make_tmap_bhnd(&tdo, dO, dtype, B * H, N, d) ||
-        !make_tmap_bhnd(&tdk, dK, dtype, B * H, Nk, d) || !make_tmap_bhnd(&tdv, dV, dtype, B * H, Nk, d))
-        return ATTN_ERR_CUDA;
-    const Workspace w = carve(workspace, B, H, N);
-    BwdParams p{};
-    p.dK = dK;
-    p.dV = dV;
-    p.key_lens = key_lens;
-    p.dev_status = dev_status;
-    p.dq_acc = w.dq_acc;
-    p.lse2 = w.lse2;
-    p.Drow = w.Drow;
-    p.B = B;
-    p.H = H;
-    p.N = N;
-    p.Nk = Nk;
-    p.Npad = npad_of(N);
-    p.nkb = (Nk + kTileRows - 1) / kTileRows;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.scale = scale;
-    p.drop_scale = 1.0f / (1.0f - dropout_p);
-    p.drop_threshold = drop_threshold(dropout_p);
-    p.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFu);
-    p.seed_hi = static_cast<uint32_t>(seed >> 32);
-    p.window = window > 0 ? window : 0;
-    return from_cuda(launch_bwd_main(tq, tk, tv, tdo, tdk, tdv, p, d, dtype == ATTN_DTYPE_FP16,
-                                     causal != 0, dropout_p > 0.f,
-                                     static_cast<cudaStream_t>(stream)));
+    return main_impl(Q, K, V, dO, dK, dV, B, dense(H, N), dense(H, Nk), d, dtype, scale, causal,
+                     window, key_lens, dropout_p, seed, workspace, dev_status, stream);
 }
 
 attn_status attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, attn_dtype dtype,
@@ -225,11 +347,7 @@ attn_status attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, attn_dtype
     if (st != ATTN_OK) return st;
     if ((st = check_math(scale, 0.f)) != ATTN_OK) return st;
     if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != ATTN_OK) return st;
-    if (!aligned16(dQ)) return ATTN_ERR_MISALIGNED;
-    const Workspace w = carve(const_cast<void*>(workspace), B, H, N);
-    return from_cuda(launch_bwd_dq_convert(dQ, w.dq_acc, B * H, N, npad_of(N), d,
-                                           dtype == ATTN_DTYPE_FP16, scale,
-                                           static_cast<cudaStream_t>(stream)));
+    return convert_impl(dQ, B, dense(H, N), d, dtype, scale, workspace, stream);
 }
 
 attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
@@ -237,25 +355,31 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
                      int d, attn_dtype dtype, float scale, int causal, int window,
                      const int32_t* key_lens, float dropout_p, uint64_t seed, void* workspace,
                      size_t workspace_bytes, int* dev_status, void* stream) {
-    // Validate everything before the first launch so that errors leave the
-    // outputs untouched.
     if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
     attn_status st = check_shape(B, H, N, d, dtype, true);
     if (st != ATTN_OK) return st;
     if ((st = check_keys(B, H, Nk, d)) != ATTN_OK) return st;
-    if ((st = check_math(scale, dropout_p)) != ATTN_OK) return st;
-    if ((st = check_workspace(workspace, workspace_bytes, B, H, N, d)) != ATTN_OK) return st;
-    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) ||
-        !aligned16(LSE) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
-        return ATTN_ERR_MISALIGNED;
-    if ((st = attn_bwd_preprocess(O, dO, LSE, B, H, N, d, dtype, workspace, workspace_bytes,
-                                  stream)) != ATTN_OK)
-        return st;
-    if ((st = attn_bwd_main(Q, K, V, dO, dK, dV, B, H, N, Nk, d, dtype, scale, causal, window, key_lens,
-                            dropout_p, seed, workspace, workspace_bytes, dev_status, stream)) !=
-        ATTN_OK)
-        return st;
-    return attn_bwd_dq_convert(dQ, B, H, N, d, dtype, scale, workspace, workspace_bytes, stream);
+    return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, dense(H, N), dense(H, Nk), d, dtype, scale,
+                    causal, window, key_lens, dropout_p, seed, workspace, workspace_bytes,
+                    dev_status, stream);
+}
+
+attn_status attn_bwd_varlen(const void* Q, const void* K, const void* V, const void* O,
+                            const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int B, int H,
+                            int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                            attn_dtype dtype, float scale, int causal, int window,
+                            float dropout_p, uint64_t seed, void* workspace,
+                            size_t workspace_bytes, int* dev_status, void* stream) {
+    if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
+    const attn_status st = check_varlen(cu_seqlens_q, cu_seqlens_k, B, H, total_q, total_k,
+                                        max_seqlen_q, max_seqlen_k, d, dtype, true);
+    if (st != ATTN_OK) return st;
+    return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B,
+                    SeqLayout{cu_seqlens_q, H, max_seqlen_q, total_q},
+                    SeqLayout{cu_seqlens_k, H, max_seqlen_k, total_k}, d, dtype, scale, causal,
+                    window, nullptr, dropout_p, seed, workspace, workspace_bytes, dev_status,
+                    stream);
 }
 
 const char* attn_status_string(attn_status status) {

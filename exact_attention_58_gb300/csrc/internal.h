@@ -13,6 +13,18 @@ namespace gbattn {
 constexpr int kTileRows = 128;
 constexpr int kFwdRowsPerCta = 2 * kTileRows;
 
+// Where the rows of a sequence live.  Dense (cu == nullptr): activations
+// [B, H, N, d] and per-row values (LSE) [B, H, N].  Packed sequences
+// (cu != nullptr): the B sequences are concatenated along the token axis,
+// activations [T, H, d] and per-row values [H, T]; sequence b holds tokens
+// [cu[b], cu[b+1]), at most N of them.
+struct SeqLayout {
+    const int32_t* cu;        // B + 1 cumulative token offsets (device), or nullptr
+    int H;
+    int N;                    // dense: rows per head; packed: longest sequence allowed
+    int total;                // packed: T tokens (unused when dense)
+};
+
 struct FwdParams {
     const void* V;            // read directly (not through TMA) on the fp32 path
     void* O;
@@ -27,6 +39,7 @@ struct FwdParams {
     uint32_t drop_threshold;  // floor(p * 2^32), clamped
     uint32_t seed_lo, seed_hi;
     int window;               // > 0: sliding window of this many keys
+    SeqLayout lq, lk;         // query / key row placement (N, Nk are their N)
 };
 
 struct BwdParams {
@@ -46,28 +59,45 @@ struct BwdParams {
     uint32_t drop_threshold;
     uint32_t seed_lo, seed_hi;
     int window;               // > 0: sliding window of this many keys
+    SeqLayout lq, lk;         // query / key row placement (N, Nk are their N)
 };
 
 // Tensor map over a contiguous [B*H][N][d] array, 128-row boxes of 128 bytes
 // along d, 128-byte swizzle.  Returns false if the driver rejected it.
 bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int BH, int N, int d);
+// Tensor map over a contiguous [T][H][d] array (packed sequences) with the
+// same boxes: 128 consecutive tokens of one head, 128 bytes along d.
+bool make_tmap_thd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int T, int H, int d);
 
 // Forward launch (validated arguments only).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int d, attn_dtype dtype, bool causal, bool dropout,
                        cudaStream_t stream);
 
+// The same for packed sequences (p.lq.cu != nullptr; bf16 or fp16).
+cudaError_t launch_fwd_packed(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const FwdParams& p, int d, attn_dtype dtype, bool causal,
+                              bool dropout, cudaStream_t stream);
+
 // Backward launches (validated arguments only).
 // f16: the 16-bit tensors are IEEE half (else bf16).
+// lq: placement of the query rows (O, dO, LSE); the workspace is
+// [B*H][Npad] rows whatever the placement.
 cudaError_t launch_bwd_pre(const void* O, const void* dO, const float* LSE, float* lse2,
-                           float* Drow, float* dq_acc, int BH, int N, int Npad, int d, bool f16,
-                           cudaStream_t stream);
+                           float* Drow, float* dq_acc, int BH, const SeqLayout& lq, int Npad,
+                           int d, bool f16, cudaStream_t stream);
 // tdk / tdv: maps over the dK / dV outputs, written with TMA stores.
 cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const BwdParams& p, int d, bool f16, bool causal, bool dropout,
                             cudaStream_t stream);
-cudaError_t launch_bwd_dq_convert(void* dQ, const float* dq_acc, int BH, int N, int Npad, int d,
-                                  bool f16, float scale, cudaStream_t stream);
+// The main launch for packed sequences (p.lq.cu != nullptr).
+cudaError_t launch_bwd_main_packed(const CUtensorMap& tq, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, const CUtensorMap& tdo,
+                                   const CUtensorMap& tdk, const CUtensorMap& tdv,
+                                   const BwdParams& p, int d, bool f16, bool causal, bool dropout,
+                                   cudaStream_t stream);
+cudaError_t launch_bwd_dq_convert(void* dQ, const float* dq_acc, int BH, const SeqLayout& lq,
+                                  int Npad, int d, bool f16, float scale, cudaStream_t stream);
 
 }  // namespace gbattn

@@ -16,6 +16,7 @@ weight is used.  Recipe for workload c (1-based):
 from __future__ import annotations
 
 import dataclasses
+import itertools
 import math
 from typing import Optional
 
@@ -116,3 +117,41 @@ def make_workload_inputs(index: int, B: Optional[int] = None, H: Optional[int] =
                        gen_seed=1000 + index, causal=w.causal, key_len_range=w.key_len_range,
                        dropout_p=w.dropout_p, dropout_seed_value=dropout_seed(index),
                        with_do=w.backward, Nk=Nk)
+
+
+@dataclasses.dataclass
+class PackedInputs:
+    q: torch.Tensor           # [total_q, H, d]
+    k: torch.Tensor           # [total_k, H, d]
+    v: torch.Tensor
+    do: torch.Tensor          # [total_q, H, d]
+    cu_q: torch.Tensor        # int32 [B + 1]
+    cu_k: torch.Tensor
+    max_q: int
+    max_k: int
+    scale: float
+    causal: bool
+    dropout_p: float
+    seed: int
+    window: int = 0
+
+
+def make_packed_inputs(lens_q, lens_k, H: int, d: int, *, dtype=torch.bfloat16,
+                       sigma: float = 1.0, gen_seed: int = 0, causal: bool = False,
+                       dropout_p: float = 0.0, dropout_seed_value: int = 0,
+                       window: int = 0) -> PackedInputs:
+    """Packed variable-length sequences: sequence b has lens_q[b] queries and
+    lens_k[b] keys.  Drawn in the order Q, K, V, dO as float32 N(0, sigma^2)
+    (dO unit variance) on a CPU generator seeded with ``gen_seed``."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(gen_seed))
+    tq, tk = int(sum(lens_q)), int(sum(lens_k))
+    q = (torch.randn((tq, H, d), generator=g, dtype=torch.float32) * sigma).to(dtype)
+    k = (torch.randn((tk, H, d), generator=g, dtype=torch.float32) * sigma).to(dtype)
+    v = (torch.randn((tk, H, d), generator=g, dtype=torch.float32) * sigma).to(dtype)
+    do = torch.randn((tq, H, d), generator=g, dtype=torch.float32).to(dtype)
+    cu = lambda lens: torch.tensor([0] + list(itertools.accumulate(int(x) for x in lens)),  # noqa: E731
+                                   dtype=torch.int32)
+    return PackedInputs(q, k, v, do, cu(lens_q), cu(lens_k), max(1, max(lens_q)),
+                        max(1, max(lens_k)), 1.0 / math.sqrt(d), causal, float(dropout_p),
+                        int(dropout_seed_value), int(window))

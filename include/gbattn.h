@@ -179,6 +179,42 @@ attn_status attn_bwd_noalloc(const void* Q, const void* K, const void* V, const 
                              int causal, int window, const int32_t* key_lens, float dropout_p,
                              uint64_t seed, int* dev_status, void* stream);
 
+/*
+ * Packed variable-length sequences (the layout of batches without padding):
+ * the B sequences of a batch are concatenated along the token axis.
+ *   Q, O, dO, dQ   [total_q, H, d]     K, V, dK, dV   [total_k, H, d]
+ *   LSE            float [H, total_q]
+ *   cu_seqlens_q   int32 [B + 1], DEVICE, 4-byte aligned: sequence b holds
+ *                  query tokens [cu_seqlens_q[b], cu_seqlens_q[b+1]);
+ *                  cu_seqlens_q[0] = 0 and cu_seqlens_q[B] = total_q.
+ *   cu_seqlens_k   the same for the keys (may equal cu_seqlens_q).
+ *   max_seqlen_q   an upper bound on every query length (sets the grid and
+ *                  the workspace); max_seqlen_k the same for the keys.
+ * Each sequence is attended on its own, with the mask of the dense entry
+ * points applied to its lengths N_b = cu_q[b+1] - cu_q[b] and
+ * Nk_b = cu_k[b+1] - cu_k[b] (queries are the last N_b key positions; no
+ * key_lens).  The dropout counter is (i, j>>2, h, b) with i, j counted within
+ * sequence b.  bf16 or fp16 only.  Offsets that leave [0, total], decrease,
+ * or give a sequence longer than its max_seqlen are clamped on the device
+ * (no access leaves the tensors) and reported as ATTN_ERR_INVALID_ARG through
+ * dev_status.  attn_bwd_varlen's workspace holds
+ * attn_bwd_workspace_size(B, H, max_seqlen_q, d) bytes.  Otherwise the
+ * conventions above hold; one launch for the forward, three for the backward.
+ */
+attn_status attn_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int B, int H, int total_q, int total_k, int max_seqlen_q,
+                            int max_seqlen_k, int d, attn_dtype dtype, float scale, int causal,
+                            int window, float dropout_p, uint64_t seed, int* dev_status,
+                            void* stream);
+attn_status attn_bwd_varlen(const void* Q, const void* K, const void* V, const void* O,
+                            const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int B, int H, int total_q, int total_k, int max_seqlen_q,
+                            int max_seqlen_k, int d, attn_dtype dtype, float scale, int causal,
+                            int window, float dropout_p, uint64_t seed, void* workspace,
+                            size_t workspace_bytes, int* dev_status, void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* attn_status_string(attn_status status);
 

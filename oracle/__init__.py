@@ -323,5 +323,42 @@ def attn_fwd_bwd_qk(Q, K, V, dO, scale=None, causal=False, key_lens=None, dropou
             dK.reshape(B, H, Nk, d), dV.reshape(B, H, Nk, d))
 
 
+def attn_fwd_bwd_varlen(Q, K, V, dO, cu_q, cu_k, scale=None, causal=False, dropout_p=0.0,
+                        seed=0, window=0, nthreads=0, _lib=None):
+    """Forward and backward over packed sequences: Q, dO [Tq, H, d], K, V
+    [Tk, H, d]; sequence b holds query rows [cu_q[b], cu_q[b+1]) and key rows
+    [cu_k[b], cu_k[b+1]) and is attended on its own (queries aligned with its
+    last keys), with dropout counters (i, j>>2, h, b) counted within the
+    sequence.  Returns O [Tq, H, d], LSE [H, Tq], dQ, dK, dV."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    Tq, H, d = Q.shape
+    Tk = K.shape[0]
+    cu_q = np.asarray(cu_q, dtype=np.int64)
+    cu_k = np.asarray(cu_k, dtype=np.int64)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    O = np.zeros((Tq, H, d))
+    LSE = np.full((H, Tq), -np.inf)
+    dQ = np.zeros((Tq, H, d))
+    dK = np.zeros((Tk, H, d))
+    dV = np.zeros((Tk, H, d))
+    for b in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+        n, nk = q1 - q0, k1 - k0
+        if n == 0 or nk == 0:   # no query, or no key: O = 0, LSE = -inf, zero gradients
+            continue
+        per_head = lambda x: np.ascontiguousarray(x.transpose(1, 0, 2))  # noqa: E731
+        o, lse, dq, dk, dv = heads_rows_fwd_bwd(
+            per_head(Q[q0:q1]), per_head(K[k0:k1]), per_head(V[k0:k1]), per_head(dO[q0:q1]),
+            np.full(H, b), np.arange(H), np.full(H, nk), scale, 0, n, causal=causal,
+            dropout_p=dropout_p, seed=seed, nthreads=nthreads, window=window, _lib=_lib)
+        O[q0:q1] = o.transpose(1, 0, 2)
+        LSE[:, q0:q1] = lse
+        dQ[q0:q1] = dq.transpose(1, 0, 2)
+        dK[k0:k1] = dk.transpose(1, 0, 2)
+        dV[k0:k1] = dv.transpose(1, 0, 2)
+    return O, LSE, dQ, dK, dV
+
+
 def num_threads() -> int:
     return int(lib().oracle_num_threads())

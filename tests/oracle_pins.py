@@ -309,6 +309,85 @@ def pin_philox_vs_triton(L) -> float:
 # ---------------------------------------------------------------------------
 # brute force and recurrence
 # ---------------------------------------------------------------------------
+def pin_varlen_equal_lengths(L) -> float:
+    """Packed sequences of one common length (queries and keys) give the
+    dense [B, H, N, d] result, dropout included (sequence b takes the dropout
+    counters of batch entry b)."""
+    worst = 0.0
+    for B, H, Nq, Nk, d, causal, p, w in ((3, 2, 9, 9, 4, True, 0.3, 0), (2, 3, 6, 11, 8, False, 0.2, 0),
+                                            (2, 2, 10, 7, 4, True, 0.0, 3)):
+        q, do = _rand(B, H, Nq, d), _rand(B, H, Nq, d)
+        k, v = _rand(B, H, Nk, d), _rand(B, H, Nk, d)
+        dense = oracle.attn_fwd_bwd_qk(q, k, v, do, 0.4, causal, None, p, 31, window=w, _lib=L)
+        pack = lambda x: np.ascontiguousarray(x.transpose(0, 2, 1, 3).reshape(-1, H, d))  # noqa: E731
+        cu_q, cu_k = np.arange(B + 1) * Nq, np.arange(B + 1) * Nk
+        O, LSE, dQ, dK, dV = oracle.attn_fwd_bwd_varlen(pack(q), pack(k), pack(v), pack(do), cu_q,
+                                                        cu_k, 0.4, causal, p, 31, window=w, _lib=L)
+        worst = max(worst, np.abs(O - pack(dense[0])).max(), np.abs(dQ - pack(dense[2])).max(),
+                    np.abs(dK - pack(dense[3])).max(), np.abs(dV - pack(dense[4])).max())
+        lse_dense = dense[1].transpose(1, 0, 2).reshape(H, -1)
+        fin = np.isfinite(lse_dense)
+        worst = max(worst, float((np.isfinite(LSE) != fin).any()),
+                    np.abs(LSE[fin] - lse_dense[fin]).max())
+    return worst
+
+
+def pin_varlen_torch(L) -> float:
+    """Packed sequences of different lengths (one without queries, one
+    without keys, one with more queries than keys) against torch float64 run
+    sequence by sequence with the mask written out, forward and autograd
+    backward, with dropout and a window."""
+    H, d, sc, seed = 2, 4, 0.5, 77
+    lens_q = [5, 0, 7, 3, 4]
+    lens_k = [9, 4, 3, 0, 6]
+    cu_q, cu_k = np.concatenate([[0], np.cumsum(lens_q)]), np.concatenate([[0], np.cumsum(lens_k)])
+    worst = 0.0
+    for causal, p, w in ((True, 0.0, 0), (False, 0.25, 0), (True, 0.15, 3)):
+        q, do = _rand(1, int(cu_q[-1]), H, d)[0], _rand(1, int(cu_q[-1]), H, d)[0]
+        k, v = _rand(1, int(cu_k[-1]), H, d)[0], _rand(1, int(cu_k[-1]), H, d)[0]
+        O, LSE, dQ, dK, dV = oracle.attn_fwd_bwd_varlen(q, k, v, do, cu_q, cu_k, sc, causal, p,
+                                                        seed, window=w, _lib=L)
+        for b in range(len(lens_q)):
+            q0, q1, k0, k1 = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+            n, nk = q1 - q0, k1 - k0
+            if n == 0:
+                continue
+            i = np.arange(n)[:, None] + (nk - n)
+            j = np.arange(nk)[None, :]
+            valid = np.ones((n, nk), dtype=bool)
+            if causal:
+                valid &= j <= i
+            if w > 0:
+                valid &= i - j < w
+                if not causal:
+                    valid &= j - i < w
+            for h in range(H):
+                tq = torch.tensor(q[q0:q1, h], requires_grad=True)
+                tk = torch.tensor(k[k0:k1, h], requires_grad=True)
+                tv = torch.tensor(v[k0:k1, h], requires_grad=True)
+                s_ = (sc * tq @ tk.T).masked_fill(~torch.as_tensor(valid), float("-inf"))
+                tl = torch.logsumexp(s_, dim=-1) if nk > 0 else torch.full((n,), float("-inf"))
+                P = torch.nan_to_num(torch.softmax(s_, dim=-1), nan=0.0)
+                if p > 0 and nk > 0:
+                    Z = oracle.dropout_mask(seed, b, h, n, nk, p, _lib=L)
+                    P = P * torch.as_tensor(Z, dtype=torch.float64) / (1 - p)
+                to = P @ tv
+                (to * torch.tensor(do[q0:q1, h])).sum().backward()
+                worst = max(worst, np.abs(O[q0:q1, h] - to.detach().numpy()).max())
+                tl = tl.detach().numpy()
+                fin = np.isfinite(tl)
+                worst = max(worst, float((np.isfinite(LSE[h, q0:q1]) != fin).any()))
+                if fin.any():
+                    worst = max(worst, np.abs(LSE[h, q0:q1][fin] - tl[fin]).max())
+                worst = max(worst, np.abs(dQ[q0:q1, h] - tq.grad.numpy()).max())
+                if nk > 0:
+                    worst = max(worst, np.abs(dK[k0:k1, h] - tk.grad.numpy()).max(),
+                                np.abs(dV[k0:k1, h] - tv.grad.numpy()).max())
+        # keys of a sequence without queries get zero gradients
+        worst = max(worst, np.abs(dK[cu_k[1]:cu_k[2]]).max(), np.abs(dV[cu_k[1]:cu_k[2]]).max())
+    return worst
+
+
 def pin_finite_differences(L, sizes=((1, 4), (5, 4), (17, 8))) -> float:
     """Central differences (h = 1e-6) of f = sum(O * dO) against the oracle's
     dQ, dK, dV; returns the worst max|g_fd - g| / max|g| over all cases."""
@@ -473,6 +552,8 @@ PINS = {
     "window_one": (pin_window_one, 1e-12),
     "window_torch": (pin_window_torch, 1e-12),
     "cross_attention_torch": (pin_cross_attention_torch, 1e-12),
+    "varlen_equal_lengths": (pin_varlen_equal_lengths, 1e-12),
+    "varlen_torch": (pin_varlen_torch, 1e-12),
     "finite_differences": (pin_finite_differences, 1e-6),
     "dk_sums_to_zero": (pin_dk_sums_to_zero, 1e-12),
     "D_equals_dO_dot_O": (pin_D_equals_dO_dot_O, 1e-12),

@@ -115,6 +115,56 @@ def test_bwd_validation(lib, kw, expected):
     assert _bwd(lib, **kw) == expected
 
 
+def _fwd_varlen(lib, **kw):
+    a = dict(ptrs=[FAKE] * 5, cu_q=FAKE, cu_k=FAKE, B=2, H=1, tq=300, tk=300, mq=200, mk=200,
+             d=64, dtype=0, scale=0.125, p=0.0)
+    a.update(kw)
+    return lib.attn_fwd_varlen(*a["ptrs"], a["cu_q"], a["cu_k"], a["B"], a["H"], a["tq"], a["tk"],
+                               a["mq"], a["mk"], a["d"], a["dtype"], a["scale"], 0, 0, a["p"], 0,
+                               None, None)
+
+
+def _bwd_varlen(lib, **kw):
+    a = dict(ptrs=[FAKE] * 9, cu_q=FAKE, cu_k=FAKE, B=2, H=1, tq=300, tk=300, mq=200, mk=200,
+             d=64, dtype=0, scale=0.125, p=0.0, ws=FAKE, ws_bytes=1 << 20)
+    a.update(kw)
+    return lib.attn_bwd_varlen(*a["ptrs"], a["cu_q"], a["cu_k"], a["B"], a["H"], a["tq"], a["tk"],
+                               a["mq"], a["mk"], a["d"], a["dtype"], a["scale"], 0, 0, a["p"], 0,
+                               a["ws"], a["ws_bytes"], None, None)
+
+
+VARLEN_CASES = [
+    (dict(cu_q=None), 1),
+    (dict(cu_k=None), 1),
+    (dict(cu_q=FAKE + 2), 3),
+    (dict(tq=0), 1),
+    (dict(tk=-1), 1),
+    (dict(mq=0), 1),
+    (dict(mk=0), 1),
+    (dict(B=0), 1),
+    (dict(d=96), 2),
+    (dict(dtype=1), 2),
+    (dict(dtype=5), 1),
+    (dict(scale=0.0), 1),
+    (dict(p=1.0), 1),
+    (dict(H=64, tq=1 << 20), 2),
+    (dict(B=4096, H=64, mq=1 << 14), 2),
+]
+
+
+@pytest.mark.parametrize("kw,expected", VARLEN_CASES + [(dict(ptrs=[FAKE] * 4 + [None]), 1),
+                                                        (dict(ptrs=[FAKE + 8] + [FAKE] * 4), 3)])
+def test_fwd_varlen_validation(lib, kw, expected):
+    assert _fwd_varlen(lib, **kw) == expected
+
+
+@pytest.mark.parametrize("kw,expected", VARLEN_CASES + [(dict(ptrs=[FAKE] * 8 + [None]), 1),
+                                                        (dict(ws=None), 4),
+                                                        (dict(ws_bytes=64), 4)])
+def test_bwd_varlen_validation(lib, kw, expected):
+    assert _bwd_varlen(lib, **kw) == expected
+
+
 def test_workspace_size(lib):
     # D and log-sum-exp (2 floats per padded row) plus the fp32 dQ accumulator
     assert ea.attn_bwd_workspace_size(2, 3, 130, 64) == 2 * 3 * 256 * (2 + 64) * 4
