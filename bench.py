@@ -16,6 +16,7 @@ host cores, and the SM clocks sampled during the timed region.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -31,7 +32,8 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from exact_attention_58_gb300.workloads import Workload, make_workload_inputs, workload  # noqa: E402
+from exact_attention_58_gb300.workloads import (Workload, dropout_seed, make_packed_inputs,  # noqa: E402
+                                                make_workload_inputs, workload)
 
 METRIC = "attention fwd/bwd TFLOP/s and % of GB300 dense bf16 tensor peak"
 DEFAULT_WORKLOAD = 3
@@ -57,6 +59,19 @@ def pairs_flops_fwd(w: Workload, window: int, Nk: int) -> float:
             hi = np.minimum(hi, t + window)
     pairs = np.maximum(0, hi - lo).sum()
     return 4.0 * w.B * w.H * w.d * float(pairs)
+
+
+def varlen_lengths(w: Workload) -> list:
+    """Packed-sequence lengths for a workload: uniform integers in [N/8, N]
+    (seeded) until the workload's B * N tokens are used up, the last one
+    cut to fit."""
+    rng = np.random.default_rng(4000 + w.N)
+    lens, left = [], w.B * w.N
+    while left > 0:
+        n = min(int(rng.integers(max(1, w.N // 8), w.N + 1)), left)
+        lens.append(n)
+        left -= n
+    return lens
 
 
 def fwd_compulsory_bytes(w: Workload) -> int:
@@ -283,44 +298,80 @@ def run_ours(args, w: Workload):
     ea.library()
 
     Nk = args.nk if args.nk > 0 else w.N
-    inp = make_workload_inputs(args.workload, Nk=Nk)
-    if args.dtype == "fp16":   # the same draws stored as IEEE half
-        for name in ("q", "k", "v", "do"):
-            t = getattr(inp, name)
-            if t is not None:
-                setattr(inp, name, t.to(torch.float32).to(torch.float16))
-    q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
     bwd = w.backward   # forward-only workloads time the forward alone
-    do = inp.do.to(dev) if bwd else None
-    kl = inp.key_lens.to(dev) if inp.key_lens is not None else None
-    B, H, N, d = q.shape
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    if bwd:
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
-        ws = torch.empty(ea.attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    kw = dict(causal=w.causal, window=args.window, key_lens=kl, dropout_p=inp.dropout_p, seed=inp.seed,
-              scale=inp.scale)
+    half = torch.float16 if args.dtype == "fp16" else None
+    lens = None
+    if args.varlen:
+        # packed sequences: lengths U[N/8, N] until B*N tokens (the workload's
+        # token budget); self-attention, the workload's mask and dtype
+        lens = varlen_lengths(w)
+        inp = make_packed_inputs(lens, lens, w.H, w.d, dtype=half or w.torch_dtype,
+                                 sigma=w.sigma, gen_seed=3000 + args.workload, causal=w.causal,
+                                 dropout_p=w.dropout_p, dropout_seed_value=dropout_seed(args.workload),
+                                 window=args.window)
+        q, k, v, do = (t.to(dev) for t in (inp.q, inp.k, inp.v, inp.do))
+        cu = inp.cu_q.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.H, q.shape[0]), dtype=torch.float32, device=dev)
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        ws = torch.empty(ea.attn_bwd_workspace_size(len(lens), w.H, inp.max_q, w.d),
+                         dtype=torch.uint8, device=dev)
+        kw = dict(causal=w.causal, window=args.window, dropout_p=inp.dropout_p, seed=inp.seed,
+                  scale=inp.scale, dev_status=status)
+        stages = [
+            ("attn_fwd_kernel",
+             lambda: ea.attn_fwd_varlen(q, k, v, cu, cu, inp.max_q, inp.max_q, out=o, lse=lse, **kw)),
+            ("attn_bwd_varlen (pre+main+convert)",
+             lambda: ea.attn_bwd_varlen(q, k, v, o, do, lse, cu, cu, inp.max_q, inp.max_q, dq=dq,
+                                        dk=dk, dv=dv, workspace=ws, **kw)),
+        ]
+    else:
+        inp = make_workload_inputs(args.workload, Nk=Nk)
+        if half is not None:   # the same draws stored as IEEE half
+            for name in ("q", "k", "v", "do"):
+                t = getattr(inp, name)
+                if t is not None:
+                    setattr(inp, name, t.to(torch.float32).to(torch.float16))
+        q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
+        do = inp.do.to(dev) if bwd else None
+        kl = inp.key_lens.to(dev) if inp.key_lens is not None else None
+        B, H, N, d = q.shape
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        if bwd:
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
+            ws = torch.empty(ea.attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+        kw = dict(causal=w.causal, window=args.window, key_lens=kl, dropout_p=inp.dropout_p,
+                  seed=inp.seed, scale=inp.scale)
+        stages = [
+            ("attn_fwd_kernel", lambda: ea.attn_fwd(q, k, v, out=o, lse=lse, dev_status=status, **kw)),
+            ("bwd_pre_kernel", lambda: ea.attn_bwd_preprocess(o, do, lse, ws)),
+            ("attn_bwd_kernel",
+             lambda: ea.attn_bwd_main(q, k, v, do, dk, dv, ws, dev_status=status, **kw)),
+            ("bwd_dq_convert_kernel", lambda: ea.attn_bwd_dq_convert(dq, ws, scale=inp.scale)),
+        ]
+    if not bwd:
+        stages = stages[:1]
+
+    def public_api():
+        """The step through the calls a user makes (attn_bwd runs the three
+        backward launches itself)."""
+        if lens is not None:
+            for _, fn in stages:
+                fn()
+            return
+        ea.attn_fwd(q, k, v, out=o, lse=lse, **kw)
+        if bwd:
+            ea.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
 
     def step(evs=None):
+        for i, (_, fn) in enumerate(stages):
+            if evs:
+                evs[i].record()
+            fn()
         if evs:
-            evs[0].record()
-        ea.attn_fwd(q, k, v, out=o, lse=lse, dev_status=status, **kw)
-        if evs:
-            evs[1].record()
-        if bwd:
-            ea.attn_bwd_preprocess(o, do, lse, ws)
-        if evs:
-            evs[2].record()
-        if bwd:
-            ea.attn_bwd_main(q, k, v, do, dk, dv, ws, dev_status=status, **kw)
-        if evs:
-            evs[3].record()
-        if bwd:
-            ea.attn_bwd_dq_convert(dq, ws, scale=inp.scale)
-        if evs:
-            evs[4].record()
+            evs[len(stages)].record()
 
     # Inputs that fit in L2 would be served from it on every step; then L2 is
     # flushed (a 256 MiB write) before each step, outside the per-stage
@@ -336,7 +387,8 @@ def run_ours(args, w: Workload):
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    ns = len(stages)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(dev.index) if rank == 0 else None
     if world > 1:
@@ -358,26 +410,36 @@ def run_ours(args, w: Workload):
         raise RuntimeError(f"device status {int(status.item())} in the timed region")
 
     elapsed_ms = start.elapsed_time(end)
-    per = [[evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps)] for i in range(4)]
+    per = [[evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps)] for i in range(ns)]
     if flush:   # the flushes are not part of the step
-        elapsed_ms = sum(evs[s][0].elapsed_time(evs[s][4]) for s in range(args.steps))
+        elapsed_ms = sum(evs[s][0].elapsed_time(evs[s][ns]) for s in range(args.steps))
     if world > 1:
         t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
 
-    exact = args.window > 0 or Nk != w.N
-    flops_fwd = pairs_flops_fwd(w, args.window, Nk) if exact else w.flops_fwd()
+    exact = args.window > 0 or Nk != w.N or lens is not None
+    if lens is not None:   # each packed sequence counted on its own
+        flops_fwd = sum(pairs_flops_fwd(dataclasses.replace(w, B=1, N=n), args.window, n)
+                        for n in lens if n > 0)
+    else:
+        flops_fwd = pairs_flops_fwd(w, args.window, Nk) if exact else w.flops_fwd()
     flops_bwd = (2.5 * flops_fwd) if bwd else 0.0
     flops_step = flops_fwd + flops_bwd
     value = world * flops_step * args.steps / (elapsed_ms * 1e-3) / 1e12
-    fwd_ms, pre_ms, main_ms, conv_ms = (statistics.mean(x) for x in per)
+    kernel_ms = {name: statistics.mean(x) for (name, _), x in zip(stages, per)}
+    fwd_ms = kernel_ms["attn_fwd_kernel"]
+    bwd_ms = sum(kernel_ms.values()) - fwd_ms
     peak, peak_sus, hbm, peak_src = load_peaks()
     fwd_tf = flops_fwd / (fwd_ms * 1e-3) / 1e12
-    bwd_tf = flops_bwd / ((pre_ms + main_ms + conv_ms) * 1e-3) / 1e12 if bwd else None
+    bwd_tf = flops_bwd / (bwd_ms * 1e-3) / 1e12 if bwd else None
+    # the backward's dominant launch: the main kernel (with pre and convert
+    # when the packed entry point times the three together)
+    bwd_main = "attn_bwd_kernel" if "attn_bwd_kernel" in kernel_ms else stages[-1][0]
+    main_ms = kernel_ms.get(bwd_main, 0.0)
     main_tf = flops_bwd / (main_ms * 1e-3) / 1e12 if bwd else None
     if bwd and main_ms >= fwd_ms:
-        dom, dom_tf, dom_ms = "attn_bwd_kernel", main_tf, main_ms
+        dom, dom_tf, dom_ms = bwd_main, main_tf, main_ms
     else:
         dom, dom_tf, dom_ms = "attn_fwd_kernel", fwd_tf, fwd_ms
     roofline = {"bound": "tensor", "kernel": dom, "achieved": dom_tf, "peak": peak,
@@ -404,9 +466,7 @@ def run_ours(args, w: Workload):
             v.copy_(hv, non_blocking=True)
             if bwd:
                 do.copy_(hdo, non_blocking=True)
-            ea.attn_fwd(q, k, v, out=o, lse=lse, **kw)
-            if bwd:
-                ea.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
+            public_api()
             ho.copy_(o, non_blocking=True)
             if bwd:
                 hdq.copy_(dq, non_blocking=True)
@@ -445,13 +505,14 @@ def run_ours(args, w: Workload):
                    "passes": "fwd+bwd" if bwd else "fwd",
                    "window": args.window if args.window > 0 else None,
                    "Nk": Nk if Nk != w.N else None,
+                   "varlen": ({"sequences": len(lens), "tokens": sum(lens), "min": min(lens),
+                               "max": max(lens)} if lens is not None else None),
                    "global_batch": world * w.B, "seq_len": w.N,
                    "parallelism": f"replicas x{world} (heads independent)",
                    "l2": l2_note},
         "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "fwd_frac_peak": fwd_tf / peak,
         "bwd_frac_peak": bwd_tf / peak if bwd else None, "peak_tflops": peak,
-        "kernel_ms": {"attn_fwd_kernel": fwd_ms, "bwd_pre_kernel": pre_ms,
-                      "attn_bwd_kernel": main_ms, "bwd_dq_convert_kernel": conv_ms},
+        "kernel_ms": kernel_ms,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": (4 if bwd else 1) * args.steps, "clocks": clocks,
     }
@@ -472,6 +533,8 @@ def main():
                     help="sliding window of this many keys (FLOPs count the attended pairs exactly)")
     ap.add_argument("--nk", type=int, default=0,
                     help="cross-attention: this many keys (queries are the last N positions)")
+    ap.add_argument("--varlen", action="store_true",
+                    help="packed variable-length sequences with the workload's token budget")
     ap.add_argument("--dtype", choices=["default", "fp16"], default="default",
                     help="fp16: store the workload's inputs as IEEE half (16-bit workloads only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
