@@ -298,9 +298,10 @@ def run_ours(args, w: Workload):
     ea.library()
 
     Nk = args.nk if args.nk > 0 else w.N
-    bwd = w.backward   # forward-only workloads time the forward alone
+    # forward-only workloads, and e4m3 inputs (forward only), time the forward alone
+    bwd = w.backward and args.dtype != "fp8"
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    half = torch.float16 if args.dtype == "fp16" else None
+    half = {"fp16": torch.float16, "fp8": getattr(torch, "float8_e4m3fn", None)}.get(args.dtype)
     lens = None
     if args.varlen:
         # packed sequences: lengths U[N/8, N] until B*N tokens (the workload's
@@ -328,16 +329,17 @@ def run_ours(args, w: Workload):
         ]
     else:
         inp = make_workload_inputs(args.workload, Nk=Nk)
-        if half is not None:   # the same draws stored as IEEE half
+        if half is not None:   # the same draws stored as IEEE half or e4m3
             for name in ("q", "k", "v", "do"):
                 t = getattr(inp, name)
                 if t is not None:
-                    setattr(inp, name, t.to(torch.float32).to(torch.float16))
+                    setattr(inp, name, t.to(torch.float32).to(half) if name != "do" or bwd else None)
         q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
         do = inp.do.to(dev) if bwd else None
         kl = inp.key_lens.to(dev) if inp.key_lens is not None else None
         B, H, N, d = q.shape
-        o = torch.empty_like(q)
+        o = torch.empty(q.shape, dtype=torch.bfloat16 if args.dtype == "fp8" else q.dtype,
+                        device=dev)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         if bwd:
             dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
@@ -442,9 +444,12 @@ def run_ours(args, w: Workload):
         dom, dom_tf, dom_ms = bwd_main, main_tf, main_ms
     else:
         dom, dom_tf, dom_ms = "attn_fwd_kernel", fwd_tf, fwd_ms
+    peak_note = f"{peak_src} bf16 dense (burst)"
+    if args.dtype == "fp8":   # e4m3 products: the bf16 figure times the nominal 2x ratio
+        peak, peak_note = 2.0 * peak, f"{peak_src} bf16 dense (burst) x 2 (nominal fp8/bf16 ratio)"
     roofline = {"bound": "tensor", "kernel": dom, "achieved": dom_tf, "peak": peak,
                 "unit": "TFLOP/s", "frac": dom_tf / peak, "traffic": recorded_traffic(dom, w.name),
-                "peak_source": f"{peak_src} bf16 dense (burst)"}
+                "peak_source": peak_note}
 
     if rank != 0:
         if world > 1:
@@ -456,7 +461,8 @@ def run_ours(args, w: Workload):
     if args.e2e_steps > 0:
         hq, hk, hv = (t.pin_memory() for t in (inp.q, inp.k, inp.v))
         hdo = inp.do.pin_memory() if bwd else None
-        ho, hdq = torch.empty_like(hq).pin_memory(), torch.empty_like(hq).pin_memory()
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hdq = torch.empty_like(hq).pin_memory()
         hdk, hdv = torch.empty_like(hk).pin_memory(), torch.empty_like(hk).pin_memory()
         s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -484,7 +490,7 @@ def run_ours(args, w: Workload):
         e_ms = s_ev.elapsed_time(e_ev)
         e2e = {"value": flops_step * args.e2e_steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": in_bytes,
-               "d2h_bytes_per_step": (2 * qbytes + 2 * kbytes) if bwd else qbytes,
+               "d2h_bytes_per_step": (2 * qbytes + 2 * kbytes) if bwd else o.numel() * o.element_size(),
                "ms_per_step": e_ms / args.e2e_steps}
 
     cpu = None
@@ -535,8 +541,9 @@ def main():
                     help="cross-attention: this many keys (queries are the last N positions)")
     ap.add_argument("--varlen", action="store_true",
                     help="packed variable-length sequences with the workload's token budget")
-    ap.add_argument("--dtype", choices=["default", "fp16"], default="default",
-                    help="fp16: store the workload's inputs as IEEE half (16-bit workloads only)")
+    ap.add_argument("--dtype", choices=["default", "fp16", "fp8"], default="default",
+                    help="fp16: store the workload's inputs as IEEE half; fp8: as e4m3, forward "
+                         "only, O in bf16 (16-bit workloads only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget-s", type=float, default=120.0)

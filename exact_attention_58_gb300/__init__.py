@@ -45,6 +45,13 @@ STATUS = {
     6: "ATTN_ERR_DEVICE_TIMEOUT",
 }
 _DTYPE = {torch.bfloat16: 0, torch.float32: 1, torch.float16: 2}
+if hasattr(torch, "float8_e4m3fn"):
+    _DTYPE[torch.float8_e4m3fn] = 3
+
+
+def _out_dtype(q: torch.Tensor):
+    """O takes q's dtype, except bf16 for e4m3 inputs."""
+    return torch.bfloat16 if _DTYPE.get(q.dtype) == 3 else q.dtype
 
 _lock = threading.Lock()
 _lib = None
@@ -180,8 +187,10 @@ def attn_fwd(q, k, v, *, causal: bool = False, window: int = 0, key_lens=None,
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
-        out = torch.empty_like(q)
-    _check_like("out", out, q)
+        out = torch.empty(q.shape, dtype=_out_dtype(q), device=q.device)
+    if out.shape != q.shape or out.dtype != _out_dtype(q) or out.device != q.device \
+            or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of q's shape (bf16 for e4m3 q)")
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     kl = _key_lens(key_lens, q)
@@ -334,8 +343,10 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
-        out = torch.empty_like(q)
-    _check_like("out", out, q)
+        out = torch.empty(q.shape, dtype=_out_dtype(q), device=q.device)
+    if out.shape != q.shape or out.dtype != _out_dtype(q) or out.device != q.device \
+            or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of q's shape (bf16 for e4m3 q)")
     if lse is None:
         lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
     st = library().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),

@@ -33,10 +33,12 @@ int npad_of(int N) { return ((N + kTileRows - 1) / kTileRows) * kTileRows; }
 // Checks shared by every entry point that takes a shape.
 attn_status check_shape(int B, int H, int N, int d, attn_dtype dtype, bool backward) {
     if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
-    if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP32 && dtype != ATTN_DTYPE_FP16)
+    if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP32 && dtype != ATTN_DTYPE_FP16 &&
+        dtype != ATTN_DTYPE_FP8_E4M3)
         return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     if (dtype == ATTN_DTYPE_FP32 && (backward || d != 64)) return ATTN_ERR_UNSUPPORTED;
+    if (dtype == ATTN_DTYPE_FP8_E4M3 && (backward || d != 128)) return ATTN_ERR_UNSUPPORTED;
     const long long elems = static_cast<long long>(B) * H * npad_of(N) * d;
     if (elems >= (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
@@ -91,16 +93,19 @@ attn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_
 
 namespace {
 
+cuuint64_t elem_bytes(attn_dtype dtype) {
+    return dtype == ATTN_DTYPE_FP32 ? 4 : (dtype == ATTN_DTYPE_FP8_E4M3 ? 1 : 2);
+}
+
 bool encode_3d(CUtensorMap* map, const void* ptr, attn_dtype dtype, const cuuint64_t dims[3],
                const cuuint64_t strides[2], const cuuint32_t box[3]) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (enc == nullptr) return false;
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapDataType ty =
-        dtype == ATTN_DTYPE_FP32
-            ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-            : (dtype == ATTN_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    CUtensorMapDataType ty = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (dtype == ATTN_DTYPE_FP32) ty = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    if (dtype == ATTN_DTYPE_FP16) ty = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (dtype == ATTN_DTYPE_FP8_E4M3) ty = CU_TENSOR_MAP_DATA_TYPE_UINT8;   // bytes moved as they are
     const CUresult r = enc(map, ty, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -110,7 +115,7 @@ bool encode_3d(CUtensorMap* map, const void* ptr, attn_dtype dtype, const cuuint
 }  // namespace
 
 bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int BH, int N, int d) {
-    const cuuint64_t es = dtype == ATTN_DTYPE_FP32 ? 4 : 2;
+    const cuuint64_t es = elem_bytes(dtype);
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es,
@@ -120,7 +125,7 @@ bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int BH,
 }
 
 bool make_tmap_thd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int T, int H, int d) {
-    const cuuint64_t es = dtype == ATTN_DTYPE_FP32 ? 4 : 2;
+    const cuuint64_t es = elem_bytes(dtype);
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                                 static_cast<cuuint64_t>(T)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es,
@@ -150,7 +155,7 @@ attn_status check_varlen(const int32_t* cu_q, const int32_t* cu_k, int B, int H,
     attn_status st = check_shape(B, H, max_q, d, dtype, backward);
     if (st != ATTN_OK) return st;
     if ((st = check_keys(B, H, max_k, d)) != ATTN_OK) return st;
-    if (dtype == ATTN_DTYPE_FP32) return ATTN_ERR_UNSUPPORTED;   // packed: 16-bit types only
+    if (dtype == ATTN_DTYPE_FP32) return ATTN_ERR_UNSUPPORTED;   // packed: 16- and 8-bit types
     if (static_cast<long long>(total_q) * H * d >= (1LL << 31) ||
         static_cast<long long>(total_k) * H * d >= (1LL << 31))
         return ATTN_ERR_UNSUPPORTED;

@@ -11,15 +11,17 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     if (p.lq.cu != nullptr) return launch_fwd_packed(tq, tk, tv, p, d, dtype, causal, dropout, stream);
     switch (dtype) {
         case ATTN_DTYPE_FP32:
-            if (d == 64) return dispatch_mask<64, true, false, false>(tq, tk, tv, p, causal, dropout, stream);
+            if (d == 64) return dispatch_mask<64, true, false, false, false>(tq, tk, tv, p, causal, dropout, stream);
             return cudaErrorInvalidValue;
         case ATTN_DTYPE_BF16:
-            if (d == 64) return dispatch_mask<64, false, false, false>(tq, tk, tv, p, causal, dropout, stream);
-            if (d == 128) return dispatch_mask<128, false, false, false>(tq, tk, tv, p, causal, dropout, stream);
+            if (d == 64) return dispatch_mask<64, false, false, false, false>(tq, tk, tv, p, causal, dropout, stream);
+            if (d == 128) return dispatch_mask<128, false, false, false, false>(tq, tk, tv, p, causal, dropout, stream);
             return cudaErrorInvalidValue;
         case ATTN_DTYPE_FP16:
-            if (d == 64) return dispatch_mask<64, false, true, false>(tq, tk, tv, p, causal, dropout, stream);
-            if (d == 128) return dispatch_mask<128, false, true, false>(tq, tk, tv, p, causal, dropout, stream);
+            if (d == 64) return dispatch_mask<64, false, true, false, false>(tq, tk, tv, p, causal, dropout, stream);
+            if (d == 128) return dispatch_mask<128, false, true, false, false>(tq, tk, tv, p, causal, dropout, stream);
+            return cudaErrorInvalidValue;        case ATTN_DTYPE_FP8_E4M3:   // output in bf16
+            if (d == 128) return dispatch_mask<128, false, false, true, false>(tq, tk, tv, p, causal, dropout, stream);
             return cudaErrorInvalidValue;
     }
     return cudaErrorInvalidValue;

@@ -41,9 +41,9 @@
 namespace gbattn {
 namespace {
 
-template <int D, bool kTF32, bool kF16>
+template <int D, bool kTF32, bool kF16, bool kFP8>
 struct FwdCfg {
-    static constexpr int ES = kTF32 ? 4 : 2;               // element bytes
+    static constexpr int ES = kTF32 ? 4 : (kFP8 ? 1 : 2);  // element bytes of Q, K, V
     static constexpr int ROWB = D * ES;                    // bytes per row
     static constexpr int NCB = ROWB / 128;                 // 128-byte column blocks
     static constexpr int BOXW = 128 / ES;                  // elements per column block
@@ -54,7 +54,7 @@ struct FwdCfg {
     static constexpr int QK_STEPS = ROWB / 32;             // MMAs per S tile
     static constexpr int PV_STEPS = kTileRows / KSTEP;     // MMAs per P V
     static constexpr int SMEM = (2 + NSLOT) * TILE + 1024 /*barriers*/ + 1024 /*align*/;
-    static constexpr uint32_t FMT = kTF32 ? kFmtTF32 : fmt16<kF16>();
+    static constexpr uint32_t FMT = kTF32 ? kFmtTF32 : (kFP8 ? kFmtE4M3 : fmt16<kF16>());
     static constexpr uint32_t IDESC_QK = idesc_f32acc(128, 128, FMT, false, false);
     static constexpr uint32_t IDESC_PV = idesc_f32acc(128, D, FMT, false, !kTF32);
     static_assert(ROWB == 128 || ROWB == 256, "tile rows must be 128 or 256 bytes");
@@ -91,12 +91,13 @@ __device__ __forceinline__ void store_v_transposed(const float* __restrict__ Vh,
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <int D, bool kTF32, bool kF16, bool kCausal, bool kDropout, bool kWindow, bool kPacked>
+template <int D, bool kTF32, bool kF16, bool kFP8, bool kCausal, bool kDropout, bool kWindow,
+          bool kPacked>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-    using C = FwdCfg<D, kTF32, kF16>;
+    using C = FwdCfg<D, kTF32, kF16, kFP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -273,8 +274,12 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                 for (int kk = 0; kk < C::QK_STEPS; ++kk) {
                     const uint32_t off = (kk >> 2) * C::CB_BYTES + (kk & 3) * 32;
-                    mma_ss<kTF32>(d_tmem, sdesc_adv(ad, off), sdesc_adv(bd, off), C::IDESC_QK,
+                    if constexpr (kFP8)
+                        mma_ss_f8(d_tmem, sdesc_adv(ad, off), sdesc_adv(bd, off), C::IDESC_QK,
                                   kk > 0 ? 1u : 0u);
+                    else
+                        mma_ss<kTF32>(d_tmem, sdesc_adv(ad, off), sdesc_adv(bd, off), C::IDESC_QK,
+                                      kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, int slot, bool accumulate) {
@@ -286,8 +291,12 @@ __global__ void __launch_bounds__(320, 1)
                     // bf16: V as stored (MN-major); fp32: V transposed (K-major)
                     const uint32_t off = kTF32 ? (kk >> 2) * (D * 128) + (kk & 3) * 32
                                                : kk * C::KSTEP * 128;
-                    mma_ts<kTF32>(d_tmem, a_tmem + kk * 8, sdesc_adv(bd, off), C::IDESC_PV,
+                    if constexpr (kFP8)
+                        mma_ts_f8(d_tmem, a_tmem + kk * 8, sdesc_adv(bd, off), C::IDESC_PV,
                                   (accumulate || kk > 0) ? 1u : 0u);
+                    else
+                        mma_ts<kTF32>(d_tmem, a_tmem + kk * 8, sdesc_adv(bd, off), C::IDESC_PV,
+                                      (accumulate || kk > 0) ? 1u : 0u);
                 }
             };
             bool ok = mbar_wait(bar_q, 0, s_abort);
@@ -446,7 +455,35 @@ __global__ void __launch_bounds__(320, 1)
                     for (int e = 0; e < 32; ++e)
                         if (32 * cc + e >= lim || 32 * cc + e < lo) sv[e] = __float_as_uint(-INFINITY);
                 }
-                if constexpr (!kTF32) {
+                if constexpr (kFP8) {
+                    // P rounded to e4m3, four keys per word, 32 keys in 8
+                    // columns; the row sum adds the unrounded P.
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {   // 4 keys per group
+                        float x[4];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[4 * g + 2 * e]),
+                                                     __uint_as_float(sv[4 * g + 2 * e + 1])),
+                                             sc2, nm2),
+                                      x[2 * e], x[2 * e + 1]);
+                            x[2 * e] = ex2_approx(x[2 * e]);
+                            x[2 * e + 1] = ex2_approx(x[2 * e + 1]);
+                            acc2[(2 * g + e) & 3] =
+                                f2_add(acc2[(2 * g + e) & 3], f2_pack(x[2 * e], x[2 * e + 1]));
+                        }
+                        uint32_t u = pack_e4m3x4(x[0], x[1], x[2], x[3]);
+                        if constexpr (kDropout) {
+                            const uint32_t keep = dropout_keep4(p.seed_lo, p.seed_hi, p.drop_threshold,
+                                                                row, k0 + 32 * cc + 4 * g, h, b);
+                            u &= ((keep & 1u) ? 0x000000FFu : 0u) | ((keep & 2u) ? 0x0000FF00u : 0u) |
+                                 ((keep & 4u) ? 0x00FF0000u : 0u) | ((keep & 8u) ? 0xFF000000u : 0u);
+                        }
+                        pk[g] = u;
+                    }
+                    tmem_st8(t_S + 8 * cc, pk);
+                } else if constexpr (!kTF32) {
                     // exp2 arguments two at a time (paired FMA); the row sum adds
                     // the bf16-rounded P in four independent paired chains.
                     uint32_t pk[16];
@@ -586,11 +623,12 @@ __global__ void __launch_bounds__(320, 1)
         atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_DEVICE_TIMEOUT));
 }
 
-template <int D, bool kTF32, bool kF16, bool kCausal, bool kDropout, bool kWindow, bool kPacked>
+template <int D, bool kTF32, bool kF16, bool kFP8, bool kCausal, bool kDropout, bool kWindow,
+          bool kPacked>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const FwdParams& p, cudaStream_t stream) {
-    using C = FwdCfg<D, kTF32, kF16>;
-    auto kern = attn_fwd_kernel<D, kTF32, kF16, kCausal, kDropout, kWindow, kPacked>;
+    using C = FwdCfg<D, kTF32, kF16, kFP8>;
+    auto kern = attn_fwd_kernel<D, kTF32, kF16, kFP8, kCausal, kDropout, kWindow, kPacked>;
     static bool configured = false;   // benign race: the attribute call is idempotent
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -602,21 +640,21 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     return cudaGetLastError();
 }
 
-template <int D, bool kTF32, bool kF16, bool kPacked, bool kWindow>
+template <int D, bool kTF32, bool kF16, bool kFP8, bool kPacked, bool kWindow>
 cudaError_t dispatch_mask_w(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, bool causal, bool dropout, cudaStream_t s) {
     if (causal)
-        return dropout ? launch_fwd_t<D, kTF32, kF16, true, true, kWindow, kPacked>(tq, tk, tv, p, s)
-                       : launch_fwd_t<D, kTF32, kF16, true, false, kWindow, kPacked>(tq, tk, tv, p, s);
-    return dropout ? launch_fwd_t<D, kTF32, kF16, false, true, kWindow, kPacked>(tq, tk, tv, p, s)
-                   : launch_fwd_t<D, kTF32, kF16, false, false, kWindow, kPacked>(tq, tk, tv, p, s);
+        return dropout ? launch_fwd_t<D, kTF32, kF16, kFP8, true, true, kWindow, kPacked>(tq, tk, tv, p, s)
+                       : launch_fwd_t<D, kTF32, kF16, kFP8, true, false, kWindow, kPacked>(tq, tk, tv, p, s);
+    return dropout ? launch_fwd_t<D, kTF32, kF16, kFP8, false, true, kWindow, kPacked>(tq, tk, tv, p, s)
+                   : launch_fwd_t<D, kTF32, kF16, kFP8, false, false, kWindow, kPacked>(tq, tk, tv, p, s);
 }
 
-template <int D, bool kTF32, bool kF16, bool kPacked>
+template <int D, bool kTF32, bool kF16, bool kFP8, bool kPacked>
 cudaError_t dispatch_mask(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const FwdParams& p, bool causal, bool dropout, cudaStream_t s) {
-    return p.window > 0 ? dispatch_mask_w<D, kTF32, kF16, kPacked, true>(tq, tk, tv, p, causal, dropout, s)
-                        : dispatch_mask_w<D, kTF32, kF16, kPacked, false>(tq, tk, tv, p, causal, dropout, s);
+    return p.window > 0 ? dispatch_mask_w<D, kTF32, kF16, kFP8, kPacked, true>(tq, tk, tv, p, causal, dropout, s)
+                        : dispatch_mask_w<D, kTF32, kF16, kFP8, kPacked, false>(tq, tk, tv, p, causal, dropout, s);
 }
 
 }  // namespace

@@ -1,5 +1,5 @@
 // attn_fwd_packed.cu — forward launch for packed variable-length sequences
-// ([T, H, d] tensors located by cumulative offsets); 16-bit types only.
+// ([T, H, d] tensors located by cumulative offsets); 16-bit and e4m3 inputs.
 #include "attn_fwd_kernel.cuh"
 
 namespace gbattn {
@@ -9,12 +9,15 @@ cudaError_t launch_fwd_packed(const CUtensorMap& tq, const CUtensorMap& tk, cons
                               bool dropout, cudaStream_t stream) {
     switch (dtype) {
         case ATTN_DTYPE_BF16:
-            if (d == 64) return dispatch_mask<64, false, false, true>(tq, tk, tv, p, causal, dropout, stream);
-            if (d == 128) return dispatch_mask<128, false, false, true>(tq, tk, tv, p, causal, dropout, stream);
+            if (d == 64) return dispatch_mask<64, false, false, false, true>(tq, tk, tv, p, causal, dropout, stream);
+            if (d == 128) return dispatch_mask<128, false, false, false, true>(tq, tk, tv, p, causal, dropout, stream);
             return cudaErrorInvalidValue;
         case ATTN_DTYPE_FP16:
-            if (d == 64) return dispatch_mask<64, false, true, true>(tq, tk, tv, p, causal, dropout, stream);
-            if (d == 128) return dispatch_mask<128, false, true, true>(tq, tk, tv, p, causal, dropout, stream);
+            if (d == 64) return dispatch_mask<64, false, true, false, true>(tq, tk, tv, p, causal, dropout, stream);
+            if (d == 128) return dispatch_mask<128, false, true, false, true>(tq, tk, tv, p, causal, dropout, stream);
+            return cudaErrorInvalidValue;
+        case ATTN_DTYPE_FP8_E4M3:   // output in bf16
+            if (d == 128) return dispatch_mask<128, false, false, true, true>(tq, tk, tv, p, causal, dropout, stream);
             return cudaErrorInvalidValue;
         default:
             return cudaErrorInvalidValue;

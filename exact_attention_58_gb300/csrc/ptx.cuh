@@ -240,6 +240,23 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
     }
 }
 
+// The same two products with 8-bit floating-point operands (kind::f8f6f4; the
+// operand formats are in the instruction descriptor).
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
 // Each lane of the warp reads 32 consecutive 32-bit columns of its own lane
 // (lane = warp's 32-lane quarter + laneid).  Results are valid after
 // tmem_ld_wait() followed by reg_fence().
@@ -346,8 +363,10 @@ __device__ __forceinline__ uint64_t sdesc_adv(uint64_t desc, uint32_t bytes) {
     return desc + static_cast<uint64_t>(bytes >> 4);
 }
 
-// Operand format codes of the instruction descriptor (A and B always share one).
-constexpr uint32_t kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2;
+// Operand format codes of the instruction descriptor (A and B always share
+// one).  kind::f16 and kind::tf32 use the first three; under kind::f8f6f4
+// code 0 means e4m3.
+constexpr uint32_t kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2, kFmtE4M3 = 0;
 
 // Instruction descriptor for kind::f16 (f16 or bf16 operands) and kind::tf32,
 // fp32 accumulator, dense: D format (bits 4-5) = f32, A and B formats (bits
@@ -462,5 +481,16 @@ __device__ __forceinline__ float h2hi_to_f32(uint32_t v) {
 }
 template <bool kF16>
 constexpr uint32_t fmt16() { return kF16 ? kFmtF16 : kFmtBF16; }
+
+// Four floats rounded to e4m3 (round to nearest even, saturating to +-448)
+// packed into one word, a in the low byte: the layout in which an 8-bit A
+// operand is read from tensor memory (consecutive K elements from the low
+// byte up).
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
 
 }  // namespace gbattn

@@ -20,7 +20,7 @@
  * ---------------------------------------
  *  Layout     Q, O, dO, dQ are contiguous [B, H, N, d] arrays and K, V, dK,
  *             dV contiguous [B, H, Nk, d] arrays, d innermost (row-major), one
- *             element type for all of them.  N is the number of query rows and
+ *             element type for all of them (O is bf16 for e4m3 inputs).  N is the number of query rows and
  *             Nk the number of keys (Nk = N for self-attention).  LSE is a
  *             contiguous float [B, H, N] array.  key_lens is an int32 [B]
  *             array.  Every pointer is a DEVICE pointer.
@@ -31,6 +31,12 @@
  *             storage and f16 x f16 products (P and dS are rounded to f16).
  *             ATTN_DTYPE_FP32: fp32 storage, TF32 products with fp32
  *             accumulation (forward only, d = 64).
+ *             ATTN_DTYPE_FP8_E4M3: Q, K, V stored as e4m3 (OCP FP8, one byte,
+ *             no infinities), e4m3 x e4m3 products with fp32 accumulation; P
+ *             is rounded to e4m3 (nearest even) for the P V product while l
+ *             and LSE use the unrounded P; O is written as bf16.  Forward
+ *             only, d = 128.  Per-tensor scales of quantised inputs are the
+ *             caller's: fold s_q * s_k into `scale` and multiply O by s_v.
  *  Shapes     d in {64, 128}; B, H, N, Nk >= 1; B*H*N*d and B*H*Nk*d
  *             < 2^31 elements per tensor.  Anything else returns ATTN_ERR_UNSUPPORTED or
  *             ATTN_ERR_INVALID_ARG: the library never falls back to another
@@ -91,18 +97,19 @@ typedef enum {
 typedef enum {
     ATTN_DTYPE_BF16 = 0,
     ATTN_DTYPE_FP32 = 1,
-    ATTN_DTYPE_FP16 = 2
+    ATTN_DTYPE_FP16 = 2,
+    ATTN_DTYPE_FP8_E4M3 = 3
 } attn_dtype;
 
 /*
  * Forward pass.
  *   Q         in   [B, H, N, d]
  *   K, V      in   [B, H, Nk, d]
- *   O         out  [B, H, N, d]  (same dtype as Q)
+ *   O         out  [B, H, N, d]  (same dtype as Q; bf16 for e4m3 Q, K, V)
  *   LSE       out  [B, H, N] float: natural log of the sum over valid keys of
  *                  exp(scale * q_i . k_j) (-inf for a row with no valid key)
- * One kernel launch.  Supported: bf16 with d in {64, 128}; fp32 (TF32
- * products) with d = 64.
+ * One kernel launch.  Supported: bf16 and fp16 with d in {64, 128}; fp32
+ * (TF32 products) with d = 64; e4m3 with d = 128.
  */
 attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                      int B, int H, int N, int Nk, int d, attn_dtype dtype, float scale,

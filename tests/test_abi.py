@@ -72,7 +72,8 @@ def _fwd(lib, **kw):
     (dict(d=256), 2),
     (dict(dtype=1, d=128), 2),
     (dict(dtype=2, d=96), 2),
-    (dict(dtype=3), 1),
+    (dict(dtype=3), 2),            # e4m3 needs d = 128
+    (dict(dtype=4), 1),
     (dict(dtype=7), 1),
     (dict(scale=0.0), 1),
     (dict(scale=float("nan")), 1),
@@ -101,7 +102,9 @@ def _bwd(lib, **kw):
     (dict(ptrs=[FAKE] * 8 + [None]), 1),
     (dict(dtype=1), 2),
     (dict(dtype=2, d=96), 2),
-    (dict(dtype=3), 1),
+    (dict(dtype=3), 2),            # e4m3: forward only
+    (dict(dtype=3, d=128), 2),
+    (dict(dtype=4), 1),
     (dict(d=80), 2),
     (dict(ws=None), 4),
     (dict(ws_bytes=16), 4),
