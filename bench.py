@@ -299,7 +299,7 @@ def run_ours(args, w: Workload):
 
     Nk = args.nk if args.nk > 0 else w.N
     # forward-only workloads, and e4m3 inputs (forward only), time the forward alone
-    bwd = w.backward and args.dtype != "fp8"
+    bwd = w.backward and args.dtype != "fp8" and w.d <= 128
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     half = {"fp16": torch.float16, "fp8": getattr(torch, "float8_e4m3fn", None)}.get(args.dtype)
     lens = None
@@ -328,7 +328,7 @@ def run_ours(args, w: Workload):
                                         dk=dk, dv=dv, workspace=ws, **kw)),
         ]
     else:
-        inp = make_workload_inputs(args.workload, Nk=Nk)
+        inp = make_workload_inputs(args.workload, Nk=Nk, d=w.d)
         if half is not None:   # the same draws stored as IEEE half or e4m3
             for name in ("q", "k", "v", "do"):
                 t = getattr(inp, name)
@@ -539,6 +539,8 @@ def main():
                     help="sliding window of this many keys (FLOPs count the attended pairs exactly)")
     ap.add_argument("--nk", type=int, default=0,
                     help="cross-attention: this many keys (queries are the last N positions)")
+    ap.add_argument("--headdim", type=int, default=0,
+                    help="override the workload's head dim (256: forward only)")
     ap.add_argument("--varlen", action="store_true",
                     help="packed variable-length sequences with the workload's token budget")
     ap.add_argument("--dtype", choices=["default", "fp16", "fp8"], default="default",
@@ -551,6 +553,8 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     w = workload(args.workload)
+    if args.headdim:
+        w = dataclasses.replace(w, d=args.headdim, name=f"{w.name}_headdim{args.headdim}")
     if args.impl == "reference":
         run_reference(args, w)
     else:

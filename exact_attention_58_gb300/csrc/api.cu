@@ -36,7 +36,9 @@ attn_status check_shape(int B, int H, int N, int d, attn_dtype dtype, bool backw
     if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP32 && dtype != ATTN_DTYPE_FP16 &&
         dtype != ATTN_DTYPE_FP8_E4M3)
         return ATTN_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+    if (d == 256 && (backward || (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP16)))
+        return ATTN_ERR_UNSUPPORTED;   // head dim 256: 16-bit forward only
     if (dtype == ATTN_DTYPE_FP32 && (backward || d != 64)) return ATTN_ERR_UNSUPPORTED;
     if (dtype == ATTN_DTYPE_FP8_E4M3 && (backward || d != 128)) return ATTN_ERR_UNSUPPORTED;
     const long long elems = static_cast<long long>(B) * H * npad_of(N) * d;
@@ -185,7 +187,6 @@ attn_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float
     p.H = lq.H;
     p.N = lq.N;
     p.Nk = lk.N;
-    p.nqb = (lq.N + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.out_scale = 1.0f / (1.0f - dropout_p);
     p.drop_threshold = drop_threshold(dropout_p);

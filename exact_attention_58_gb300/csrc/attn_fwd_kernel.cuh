@@ -49,18 +49,28 @@ struct FwdCfg {
     static constexpr int BOXW = 128 / ES;                  // elements per column block
     static constexpr int TILE = kTileRows * ROWB;          // bytes per 128-row tile
     static constexpr int CB_BYTES = kTileRows * 128;       // bytes per column block
-    static constexpr int NSLOT = (ROWB == 128) ? 8 : 4;    // K/V ring slots
+    // Query tiles per CTA: two tiles share each K/V block in one CTA, or one
+    // tile per CTA with two CTAs resident on an SM.  d = 256 takes one tile:
+    // its O accumulator alone fills half of tensor memory.
+    static constexpr int TILES = D == 256 ? 1 : kFwdTilesPerCta;
+    static constexpr int NSLOT = (TILES == 2 ? 4 : 2) * ((ROWB == 128) ? 2 : 1);   // K/V ring slots
+    static constexpr int THREADS = 32 * (4 * TILES + 2);   // softmax warps, producer, MMA
+    static constexpr int PRODUCER_WARP = 4 * TILES;
+    static constexpr int MMA_WARP = 4 * TILES + 1;
+    static constexpr uint32_t TMEM_COLS = (TILES == 2 || D > 128) ? 512 : 256;
+    static constexpr int CTAS_PER_SM = TMEM_COLS == 512 ? 1 : 2;
+    static constexpr uint32_t O_COL = 128 * TILES;          // first O column (S tiles below)
     static constexpr int KSTEP = 32 / ES;                  // K elements per MMA
     static constexpr int QK_STEPS = ROWB / 32;             // MMAs per S tile
     static constexpr int PV_STEPS = kTileRows / KSTEP;     // MMAs per P V
-    static constexpr int SMEM = (2 + NSLOT) * TILE + 1024 /*barriers*/ + 1024 /*align*/;
+    static constexpr int SMEM = (TILES + NSLOT) * TILE + 1024 /*barriers*/ + 1024 /*align*/;
     static constexpr uint32_t FMT = kTF32 ? kFmtTF32 : (kFP8 ? kFmtE4M3 : fmt16<kF16>());
     static constexpr uint32_t IDESC_QK = idesc_f32acc(128, 128, FMT, false, false);
     static constexpr uint32_t IDESC_PV = idesc_f32acc(128, D, FMT, false, !kTF32);
-    static_assert(ROWB == 128 || ROWB == 256, "tile rows must be 128 or 256 bytes");
+    static_assert(ROWB == 128 || ROWB == 256 || ROWB == 512, "tile rows of 128, 256 or 512 bytes");
+    static_assert(O_COL + TILES * D <= TMEM_COLS, "S and O tiles must fit in tensor memory");
 };
 
-constexpr uint32_t kTmemCols = 512;
 
 // fp32 V_j (keys k0..k0+127 of one head, [N][D] in global memory) written into
 // a shared-memory slot as the K-major B operand of O += P V: D rows (one per
@@ -93,7 +103,8 @@ constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int D, bool kTF32, bool kF16, bool kFP8, bool kCausal, bool kDropout, bool kWindow,
           bool kPacked>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
+                                  FwdCfg<D, kTF32, kF16, kFP8>::CTAS_PER_SM)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -101,9 +112,9 @@ __global__ void __launch_bounds__(320, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sQ = smem;                                   // 2 tiles
-    uint8_t* sKV = smem + 2 * C::TILE;                    // NSLOT tiles
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (2 + C::NSLOT) * C::TILE);
+    uint8_t* sQ = smem;                                   // C::TILES tiles
+    uint8_t* sKV = smem + C::TILES * C::TILE;             // NSLOT tiles
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (C::TILES + C::NSLOT) * C::TILE);
     uint64_t* bar_q = bars;
     uint64_t* full = bars + 1;
     uint64_t* empty = full + C::NSLOT;
@@ -140,7 +151,7 @@ __global__ void __launch_bounds__(320, 1)
         if (raw != L && threadIdx.x == 0 && p.dev_status != nullptr)
             atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_INVALID_ARG));
     }
-    const int q0 = qb * kFwdRowsPerCta;
+    const int q0 = qb * kTileRows * C::TILES;
     const int nkv_all = (L + kTileRows - 1) / kTileRows;
     // > 0: sliding window, keys with row - key < W (and key - row < W unless
     // causal); a compile-time 0 in the instantiations without a window
@@ -153,7 +164,7 @@ __global__ void __launch_bounds__(320, 1)
     for (int t = 0; t < 2; ++t) {
         const int first = q0 + t * kTileRows;
         int lo = 0, hi = 0;
-        if (first < N) {
+        if (first < N && t < C::TILES) {
             const int last = min(first + kTileRows - 1, N - 1);
             hi = kCausal ? (last + off >= 0 ? min(nkv_all, (last + off) / kTileRows + 1) : 0)
                          : nkv_all;
@@ -189,8 +200,8 @@ __global__ void __launch_bounds__(320, 1)
         *s_abort = 0;
         fence_mbar_init();
     }
-    if (warp == 9) {
-        tmem_alloc(s_tmem, kTmemCols);
+    if (warp == C::MMA_WARP) {
+        tmem_alloc(s_tmem, C::TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -198,7 +209,7 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    if (warp == 8) {
+    if (warp == C::PRODUCER_WARP) {
         // ================= TMA producer =================
         // The whole warp walks the ring (waits are warp-collective); lane 0
         // issues the TMA copies.  TF32 products only take a K-major B, so for
@@ -259,7 +270,7 @@ __global__ void __launch_bounds__(320, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 9) {
+    } else if (warp == C::MMA_WARP) {
         // ================= MMA issuer =================
         if (lane == 0 && nkv > 0) {
             // Descriptor bases built once; each MMA only adds a constant.
@@ -283,7 +294,7 @@ __global__ void __launch_bounds__(320, 1)
                 }
             };
             auto issue_pv = [&](int t, int slot, bool accumulate) {
-                const uint32_t d_tmem = tmem + 256u + D * t;
+                const uint32_t d_tmem = tmem + C::O_COL + D * t;
                 const uint32_t a_tmem = tmem + 128u * t;
                 const uint64_t bd = sdesc_adv(dv0, slot * C::TILE);
 #pragma unroll
@@ -313,7 +324,7 @@ __global__ void __launch_bounds__(320, 1)
                 const uint32_t next_v_phase = (seq / C::NSLOT) & 1;
                 ++seq;
                 bool k_ready = false;
-                for (int t = 0; t < 2 && ok; ++t) {
+                for (int t = 0; t < C::TILES && ok; ++t) {
                     const bool qk = j >= jlo(t) && j < jhi(t);
                     const bool prev = j - 1 >= jlo(t) && j - 1 < jhi(t);   // tile t saw block j-1
                     const bool last_pv = prev && j == jhi(t);
@@ -346,7 +357,7 @@ __global__ void __launch_bounds__(320, 1)
                 v_phase = next_v_phase;
                 v_ready = false;
             }
-            for (int t = 0; t < 2 && ok; ++t) {   // tiles whose last block is the CTA's last
+            for (int t = 0; t < C::TILES && ok; ++t) {   // tiles whose last block is the CTA's last
                 if (nkv_t(t) == 0 || jhi(t) != jbeg + nkv) continue;
                 ok = mbar_wait(&bar_p[t], (jhi(t) - 1 - jlo(t)) & 1, s_abort);
                 if (ok && !v_ready) {
@@ -374,7 +385,7 @@ __global__ void __launch_bounds__(320, 1)
         const int tile_first_row = q0 + t * kTileRows;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const uint32_t t_S = t_lane + 128u * t;
-        const uint32_t t_O = t_lane + 256u + D * t;
+        const uint32_t t_O = t_lane + C::O_COL + D * t;
         float m_ref = -INFINITY;   // reference max, log2 units of scaled scores
         float l = 0.f;
         bool ok = true;
@@ -618,7 +629,7 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 9) tmem_dealloc(tmem, kTmemCols);
+    if (warp == C::MMA_WARP) tmem_dealloc(tmem, C::TMEM_COLS);
     if (threadIdx.x == 0 && *s_abort && p.dev_status != nullptr)
         atomicCAS(p.dev_status, 0, static_cast<int>(ATTN_ERR_DEVICE_TIMEOUT));
 }
@@ -635,8 +646,10 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const unsigned grid = static_cast<unsigned>(p.nqb) * static_cast<unsigned>(p.B * p.H);
-    kern<<<grid, 320, C::SMEM, stream>>>(tq, tk, tv, p);
+    FwdParams pp = p;
+    pp.nqb = (p.N + kTileRows * C::TILES - 1) / (kTileRows * C::TILES);
+    const unsigned grid = static_cast<unsigned>(pp.nqb) * static_cast<unsigned>(p.B * p.H);
+    kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, pp);
     return cudaGetLastError();
 }
 

@@ -11,10 +11,12 @@ cudaError_t launch_fwd_packed(const CUtensorMap& tq, const CUtensorMap& tk, cons
         case ATTN_DTYPE_BF16:
             if (d == 64) return dispatch_mask<64, false, false, false, true>(tq, tk, tv, p, causal, dropout, stream);
             if (d == 128) return dispatch_mask<128, false, false, false, true>(tq, tk, tv, p, causal, dropout, stream);
+            if (d == 256) return dispatch_mask<256, false, false, false, true>(tq, tk, tv, p, causal, dropout, stream);
             return cudaErrorInvalidValue;
         case ATTN_DTYPE_FP16:
             if (d == 64) return dispatch_mask<64, false, true, false, true>(tq, tk, tv, p, causal, dropout, stream);
             if (d == 128) return dispatch_mask<128, false, true, false, true>(tq, tk, tv, p, causal, dropout, stream);
+            if (d == 256) return dispatch_mask<256, false, true, false, true>(tq, tk, tv, p, causal, dropout, stream);
             return cudaErrorInvalidValue;
         case ATTN_DTYPE_FP8_E4M3:   // output in bf16
             if (d == 128) return dispatch_mask<128, false, false, true, true>(tq, tk, tv, p, causal, dropout, stream);

@@ -9,9 +9,9 @@
 
 namespace gbattn {
 
-// Rows per query / key tile (the MMA's M) and per forward CTA (two tiles).
+// Rows per query / key tile (the MMA's M) and query tiles per forward CTA.
 constexpr int kTileRows = 128;
-constexpr int kFwdRowsPerCta = 2 * kTileRows;
+constexpr int kFwdTilesPerCta = 2;
 
 // Where the rows of a sequence live.  Dense (cu == nullptr): activations
 // [B, H, N, d] and per-row values (LSE) [B, H, N].  Packed sequences
@@ -33,7 +33,7 @@ struct FwdParams {
     int* dev_status;
     int B, H, N;              // N: query rows
     int Nk;                   // keys (N_k != N: cross-attention)
-    int nqb;                  // query blocks of kFwdRowsPerCta rows
+    int nqb;                  // query blocks of one forward CTA (set by the launch)
     float scale_log2;         // scale * log2(e)
     float out_scale;          // 1 / (1 - dropout_p)
     uint32_t drop_threshold;  // floor(p * 2^32), clamped

@@ -109,11 +109,12 @@ def make_inputs(B: int, H: int, N: int, d: int, *, dtype=torch.bfloat16, sigma: 
 
 
 def make_workload_inputs(index: int, B: Optional[int] = None, H: Optional[int] = None,
-                         N: Optional[int] = None, Nk: Optional[int] = None) -> Inputs:
-    """Inputs of workload ``index`` (1-based), optionally with B/H/N cut down
-    or with ``Nk`` keys (cross-attention) instead of N."""
+                         N: Optional[int] = None, Nk: Optional[int] = None,
+                         d: Optional[int] = None) -> Inputs:
+    """Inputs of workload ``index`` (1-based), optionally with B/H/N cut down,
+    with ``Nk`` keys (cross-attention) instead of N, or another head dim."""
     w = workload(index)
-    return make_inputs(B or w.B, H or w.H, N or w.N, w.d, dtype=w.torch_dtype, sigma=w.sigma,
+    return make_inputs(B or w.B, H or w.H, N or w.N, d or w.d, dtype=w.torch_dtype, sigma=w.sigma,
                        gen_seed=1000 + index, causal=w.causal, key_len_range=w.key_len_range,
                        dropout_p=w.dropout_p, dropout_seed_value=dropout_seed(index),
                        with_do=w.backward, Nk=Nk)

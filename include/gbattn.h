@@ -37,7 +37,8 @@
  *             and LSE use the unrounded P; O is written as bf16.  Forward
  *             only, d = 128.  Per-tensor scales of quantised inputs are the
  *             caller's: fold s_q * s_k into `scale` and multiply O by s_v.
- *  Shapes     d in {64, 128}; B, H, N, Nk >= 1; B*H*N*d and B*H*Nk*d
+ *  Shapes     d in {64, 128} (and 256 for the bf16 and fp16 forward);
+ *             B, H, N, Nk >= 1; B*H*N*d and B*H*Nk*d
  *             < 2^31 elements per tensor.  Anything else returns ATTN_ERR_UNSUPPORTED or
  *             ATTN_ERR_INVALID_ARG: the library never falls back to another
  *             implementation.
@@ -108,7 +109,7 @@ typedef enum {
  *   O         out  [B, H, N, d]  (same dtype as Q; bf16 for e4m3 Q, K, V)
  *   LSE       out  [B, H, N] float: natural log of the sum over valid keys of
  *                  exp(scale * q_i . k_j) (-inf for a row with no valid key)
- * One kernel launch.  Supported: bf16 and fp16 with d in {64, 128}; fp32
+ * One kernel launch.  Supported: bf16 and fp16 with d in {64, 128, 256}; fp32
  * (TF32 products) with d = 64; e4m3 with d = 128.
  */
 attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
