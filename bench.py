@@ -105,7 +105,8 @@ def load_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("attn_fwd.cu", "attn_bwd.cu", "ptx.cuh", "philox.cuh"):
+    for name in ("attn_fwd_kernel.cuh", "attn_fwd.cu", "attn_bwd_kernel.cuh", "attn_bwd.cu",
+                 "ptx.cuh", "philox.cuh", "seq.cuh", "internal.h"):
         with open(os.path.join(ROOT, "exact_attention_58_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
