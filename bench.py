@@ -243,6 +243,27 @@ def cpu_baseline(inp, w, target_s=15.0):
 
 
 # ---------------------------------------------------------------------------
+# several ranks: independent replicas, timed by the slowest
+# ---------------------------------------------------------------------------
+def max_over_ranks(x: float, device) -> float:
+    """The largest x over the ranks of the default process group (x itself
+    when there is none): the job's time is its slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_rank_step: float, steps: int, elapsed_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank ran `steps` steps of its own replica in
+    (at most) elapsed_ms."""
+    return world * flops_per_rank_step * steps / (elapsed_ms * 1e-3) / 1e12
+
+
+# ---------------------------------------------------------------------------
 # reference arm: the oracle, as it stands, on the host cores
 # ---------------------------------------------------------------------------
 def run_reference(args, w: Workload):
@@ -416,10 +437,7 @@ def run_ours(args, w: Workload):
     per = [[evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps)] for i in range(ns)]
     if flush:   # the flushes are not part of the step
         elapsed_ms = sum(evs[s][0].elapsed_time(evs[s][ns]) for s in range(args.steps))
-    if world > 1:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     exact = args.window > 0 or Nk != w.N or lens is not None
     if lens is not None:   # each packed sequence counted on its own
@@ -429,7 +447,7 @@ def run_ours(args, w: Workload):
         flops_fwd = pairs_flops_fwd(w, args.window, Nk) if exact else w.flops_fwd()
     flops_bwd = (2.5 * flops_fwd) if bwd else 0.0
     flops_step = flops_fwd + flops_bwd
-    value = world * flops_step * args.steps / (elapsed_ms * 1e-3) / 1e12
+    value = job_tflops(world, flops_step, args.steps, elapsed_ms)
     kernel_ms = {name: statistics.mean(x) for (name, _), x in zip(stages, per)}
     fwd_ms = kernel_ms["attn_fwd_kernel"]
     bwd_ms = sum(kernel_ms.values()) - fwd_ms
