@@ -23,7 +23,11 @@ namespace {
 //   dQ_i += dS K_j            (smem x smem, added into the fp32 workspace)
 //   dV_j += (P Z/(1-p))^T dO_i                           (P read from TMEM)
 //   dK_j += dS^T Q_i                                     (dS read from smem)
-// dK_j (times scale) and dV_j leave the chip once, at the end.
+// dK_j (times scale) and dV_j leave the chip once, at the end.  Queries stand
+// at key positions i + Nk - N (cross-attention), which shifts the causal and
+// window bounds of the query-block range; rows of a packed sequence are
+// located through seq.cuh, and the last key block of a packed sequence writes
+// dK, dV row by row so that nothing lands in the next sequence's rows.
 //
 // Warp roles (448 threads):
 //   warps 0-3  compute, query columns 0-63 of the block: one thread per key

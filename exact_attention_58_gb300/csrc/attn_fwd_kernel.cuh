@@ -1,23 +1,29 @@
 // attn_fwd_kernel.cuh — fused exact-attention forward for sm_103a.
 //
 // One CTA owns 256 query rows (two 128-row tiles, A and B) of one (b, h) head
-// and walks the key/value sequence in 128-row blocks, keeping everything on
-// chip: the online-softmax recurrence of "Why FlashAttention Is a Kernel
-// Story" (section "Tiling": running row max m, running denominator l, output
-// rescaled when m grows, O / l at the end) with S = Q K^T and O += P V on the
-// tcgen05 tensor cores.  Only O and the per-row log-sum-exp reach HBM.
+// — one 128-row tile at head dim 256, whose fp32 O alone takes 256 tensor-
+// memory columns — and walks the key/value sequence in 128-row blocks,
+// keeping everything on chip: the online-softmax recurrence of "Why
+// FlashAttention Is a Kernel Story" (section "Tiling": running row max m,
+// running denominator l, output rescaled when m grows, O / l at the end) with
+// S = Q K^T and O += P V on the tcgen05 tensor cores.  Only O and the per-row
+// log-sum-exp reach HBM.  Queries stand at key positions i + Nk - N (cross-
+// attention); a sequence's rows are placed densely or packed (seq.cuh).
 //
-// Warp roles (320 threads):
-//   warps 0-3  softmax for tile A, one thread per query row (TMEM lane)
-//   warps 4-7  softmax for tile B
-//   warp  8    TMA producer: Q once, then K_j, V_j into a ring of smem slots
-//   warp  9    MMA issuer: S_t = Q_t K_j^T (both operands in smem) and
-//              O_t += P_t V_j (P read from tensor memory, V from smem)
+// Warp roles (320 threads with two tiles, 192 with one):
+//   warps 0-3   softmax for tile A, one thread per query row (TMEM lane)
+//   warps 4-7   softmax for tile B (two tiles only)
+//   next warp   TMA producer: Q once, then K_j, V_j into a ring of smem slots
+//   last warp   MMA issuer: S_t = Q_t K_j^T (both operands in smem) and
+//               O_t += P_t V_j (P read from tensor memory, V from smem), as
+//               kind::f16, kind::tf32 or kind::f8f6f4 products by input type
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
-//   [0,128)   S_A, later P_A (bf16 pairs in the first 64 columns, or fp32)
+//   [0,128)   S_A, later P_A (16-bit pairs in the first 64 columns, e4m3
+//             quads in the first 32, or fp32)
 //   [128,256) S_B / P_B
 //   [256, 256+d) O_A,  [256+d, 256+2d) O_B   (fp32 accumulators)
+//   one tile: S in [0,128), O in [128, 128+d)
 // P aliases S: the MMA warp issues S_t(j+1) only after O_t += P_t(j) V_j,
 // and tcgen05 MMAs from one thread execute in issue order.
 //
