@@ -136,3 +136,30 @@ def test_fp8_precision_study():
           f"bf16 vs oracle: rms {rms16:.3e} max {np.abs(e16).max():.3e}")
     assert np.abs(e16).max() <= O_ATOL
     assert rms8 <= 2.0**-4 * math.sqrt(float((O_ref**2).mean())) + 1e-3
+
+
+def test_fp8_packed_sequences():
+    """e4m3 packed variable-length sequences, each sequence checked against
+    the rounding bound on its own lengths."""
+    from exact_attention_58_gb300.workloads import make_packed_inputs
+    lens = [150, 33, 300]
+    inp = make_packed_inputs(lens, lens, 2, 128, dtype=FP8, gen_seed=808, causal=True)
+    q, k, v = (t.cuda() for t in (inp.q, inp.k, inp.v))
+    cu = inp.cu_q.cuda()
+    o, lse = ea.attn_fwd_varlen(q, k, v, cu, cu, inp.max_q, inp.max_k, causal=True,
+                                scale=inp.scale)
+    torch.cuda.synchronize()
+    assert o.dtype == torch.bfloat16
+    qd, kd, vd = f64(inp.q), f64(inp.k), f64(inp.v)
+    O_ref, L_ref, _, _, _ = oracle.attn_fwd_bwd_varlen(qd, kd, vd, np.zeros_like(qd),
+                                                       inp.cu_q.numpy(), inp.cu_k.numpy(),
+                                                       inp.scale, True)
+    cuq = inp.cu_q.numpy()
+    for b in range(len(lens)):
+        s0, s1 = int(cuq[b]), int(cuq[b + 1])
+        for h in range(2):
+            bound = rounding_bound(qd[s0:s1, h], kd[s0:s1, h], vd[s0:s1, h], inp.scale, True,
+                                   s1 - s0, 0, 0.0, 0, b, h)
+            err = np.abs(f64(o[s0:s1, h]) - O_ref[s0:s1, h])
+            assert (err <= bound + 2.0**-8 * np.abs(O_ref[s0:s1, h]) + 1e-3).all()
+            assert lse_err(f64(lse[h, s0:s1]), L_ref[h, s0:s1]) <= 4e-3
