@@ -118,3 +118,26 @@ def test_varlen_full_size_sampled_sequences():
         assert lse_err(f64(lse[:, s0:s1]), L_ref) <= 4e-3
         for g, ref in ((dq, dQ), (dk, dK), (dv, dV)):
             assert grad_err(sl(g), ref) <= GRAD_RTOL
+
+
+def test_varlen_bad_offsets_are_clamped_and_reported():
+    """Decreasing offsets and a sequence longer than max_seqlen: every access
+    stays inside the tensors (the kernels clamp each sequence to [0, T] and
+    to max_seqlen) and dev_status reports ATTN_ERR_INVALID_ARG."""
+    H, d = 2, 64
+    T = 400
+    q, k, v = (torch.randn(T, H, d, dtype=torch.bfloat16, device="cuda") for _ in range(3))
+    cu = torch.tensor([0, 300, 200, 400], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, lse = ea.attn_fwd_varlen(q, k, v, cu, cu, 256, 256, causal=True, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1   # ATTN_ERR_INVALID_ARG
+    assert torch.isfinite(o[:256].float()).all()
+    do = torch.randn(T, H, d, dtype=torch.bfloat16, device="cuda")
+    status2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dq, dk, dv = ea.attn_bwd_varlen(q, k, v, o, do, lse, cu, cu, 256, 256, causal=True,
+                                    dev_status=status2)
+    torch.cuda.synchronize()
+    assert int(status2.item()) == 1
+    for g in (dq, dk, dv):
+        assert torch.isfinite(g[:256].float()).all()
