@@ -163,3 +163,17 @@ def test_fp8_packed_sequences():
             err = np.abs(f64(o[s0:s1, h]) - O_ref[s0:s1, h])
             assert (err <= bound + 2.0**-8 * np.abs(O_ref[s0:s1, h]) + 1e-3).all()
             assert lse_err(f64(lse[h, s0:s1]), L_ref[h, s0:s1]) <= 4e-3
+
+
+def test_fp8_spiky_keys_move_the_row_max():
+    """The e4m3 path with keys of the last 32-key chunk of every block scaled
+    up six-fold (the values stay in the e4m3 range): large jumps of the row
+    max and its rescale of O and l."""
+    inp = make_inputs(2, 2, 400, 128, dtype=torch.float32, gen_seed=77, causal=False,
+                      with_do=False)
+    j = np.arange(400)
+    spike = torch.from_numpy(((j % 128) // 32) == 3)
+    inp.k[:, :, spike] *= 6.0
+    for name in ("q", "k", "v"):
+        setattr(inp, name, getattr(inp, name).to(FP8))
+    _check(inp)

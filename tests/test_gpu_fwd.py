@@ -147,3 +147,19 @@ def test_no_nxn_buffer_long_sequence():
     torch.cuda.synchronize()
     extra = torch.cuda.max_memory_allocated() - base
     assert extra < 64 * 2**20, extra
+
+
+@pytest.mark.parametrize("chunk", [1, 2, 3])
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
+def test_spiky_keys_move_the_row_max(chunk, d, causal):
+    """Keys of one 32-key chunk of every 128-key block scaled up six-fold, so
+    that a row's maximum jumps by far more than the lazy-rescale threshold
+    from one block to the next (the rescale of O and l) and varies strongly
+    inside a block."""
+    inp = make_inputs(2, 2, 520, d, gen_seed=7000 + 10 * chunk + d, causal=causal, with_do=False)
+    j = np.arange(inp.k.shape[2])
+    spike = torch.from_numpy(((j % 128) // 32) == chunk)
+    k = inp.k.float()
+    k[:, :, spike] *= 6.0
+    inp.k = k.to(inp.q.dtype)
+    _check(inp)
