@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
                     tmem_st8(t_S + 8 * cc, pk);
                 } else if constexpr (!kTF32) {
                     // exp2 arguments two at a time (paired FMA); the row sum adds
-                    // the bf16-rounded P in four independent paired chains.
+                    // the unrounded P (fp32) in four independent paired chains.
                     uint32_t pk[16];
 #pragma unroll
                     for (int g = 0; g < 8; ++g) {   // 4 keys per group
@@ -517,9 +517,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
                                                      __uint_as_float(sv[4 * g + 2 * e + 1])),
                                              sc2, nm2),
                                       x0, x1);
-                            uint32_t u = pack_h2<kF16>(ex2_approx(x0), ex2_approx(x1));
-                            acc2[(2 * g + e) & 3] = f2_add(
-                                acc2[(2 * g + e) & 3], f2_pack(h2lo_to_f32<kF16>(u), h2hi_to_f32<kF16>(u)));
+                            x0 = ex2_approx(x0);
+                            x1 = ex2_approx(x1);
+                            uint32_t u = pack_h2<kF16>(x0, x1);
+                            acc2[(2 * g + e) & 3] = f2_add(acc2[(2 * g + e) & 3], f2_pack(x0, x1));
                             if constexpr (kDropout) {
                                 const uint32_t km = ((keep >> (2 * e)) & 1u ? 0x0000FFFFu : 0u) |
                                                     ((keep >> (2 * e + 1)) & 1u ? 0xFFFF0000u : 0u);
