@@ -417,8 +417,8 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
 
             // ---- pass 1: row max (S read from TMEM, eight independent chains) ----
             float mx;
+            uint32_t sr[4][32];   // chunk 0 stays live into pass 2
             {
-                uint32_t sr[4][32];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) tmem_ld32(t_S + 32 * c, sr[c]);
                 tmem_ld_wait();
@@ -451,8 +451,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
             }
             const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
-            // ---- pass 2: P = exp2(s scale log2e - m), chunk by chunk (S re-read
-            // from TMEM, next chunk's load overlapping this chunk's math) ----
+            // ---- pass 2: P = exp2(s scale log2e - m), chunk by chunk: chunk 0
+            // of S from pass 1's registers, chunks 1-3 re-read from TMEM, each
+            // load overlapping the previous chunk's math (P of chunk c lands in
+            // columns below 32 (c + 1), clear of the chunks still to be read) ----
             float rowsum = 0.f;
             const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
             const uint64_t nm2 = f2_pack(neg_m, neg_m);
@@ -460,14 +462,12 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
 #pragma unroll
             for (int k = 0; k < 4; ++k) acc2[k] = f2_pack(0.f, 0.f);
             uint32_t buf[2][32];
-            tmem_ld32(t_S, buf[0]);
-            tmem_ld_wait();
-            reg_fence(buf[0]);
+            tmem_ld32(t_S + 32, buf[1]);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-                if (cc < 3) tmem_ld32(t_S + 32 * (cc + 1), buf[(cc + 1) & 1]);
-                uint32_t* sv = buf[cc & 1];
-                if (tile_mask) {
+                if (cc >= 1 && cc < 3) tmem_ld32(t_S + 32 * (cc + 1), buf[(cc + 1) & 1]);
+                uint32_t* sv = cc == 0 ? sr[0] : buf[cc & 1];
+                if (tile_mask && cc >= 1) {   // chunk 0 was masked in pass 1
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
                         if (32 * cc + e >= lim || 32 * cc + e < lo) sv[e] = __float_as_uint(-INFINITY);
