@@ -388,6 +388,7 @@ __global__ void __launch_bounds__(448, 1)
         const uint32_t tS = tl + C::C_S + 64 * hh;
         const uint32_t tdP = tl + C::C_DP + 64 * hh;   // this half's dP^T columns
         const bool row_valid = j < L;
+        const int jo = j - off;   // this key's position on the query axis
         uint8_t* rowp = smem + C::OFF_DS + hh * C::CB_BYTES + r * 128;
         bool ok = true;
         for (int it = 0; it < nq; ++it) {
@@ -462,8 +463,8 @@ __global__ void __launch_bounds__(448, 1)
                         float x = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), p.scale_log2,
                                                   -lv[2 * e + u]));
                         const int iq = q0h + col;   // query index
-                        const bool valid = row_valid && (!diag || j <= iq + off) &&
-                                           (!wmask || (iq + off - j < W && (kCausal || j - iq - off < W)));
+                        const bool valid = row_valid && (!diag || jo <= iq) &&
+                                           (!wmask || (iq - jo < W && (kCausal || jo - iq < W)));
                         x = valid ? x : 0.f;
                         pr[col] = x;
                         pd[u] = x;
