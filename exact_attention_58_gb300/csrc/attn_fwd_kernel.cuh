@@ -334,14 +334,16 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
                     const bool qk = j >= jlo(t) && j < jhi(t);
                     const bool prev = j - 1 >= jlo(t) && j - 1 < jhi(t);   // tile t saw block j-1
                     const bool last_pv = prev && j == jhi(t);
-                    if (prev) {   // O_t += P_t(j-1) V_{j-1}
+                    if (prev) {   // O_t += P_t(j-1) V_{j-1}, once the softmax of j-1 is done
                         ok = mbar_wait(&bar_p[t], (j - 1 - jlo(t)) & 1, s_abort);
-                        if (ok && !v_ready) {
-                            ok = mbar_wait(&full[v_slot], v_phase, s_abort);
-                            v_ready = true;
-                        }
                         if (!ok) break;
                         tc_fence_after();
+                        if (!v_ready) {
+                            ok = mbar_wait(&full[v_slot], v_phase, s_abort);
+                            v_ready = true;
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
                         issue_pv(t, v_slot, j - 1 > jlo(t));
                         if (last_pv) tc_commit(&bar_o[t]);
                     }
