@@ -593,14 +593,19 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
         if (ok) {
             const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
             const size_t row_off = act_offset_t<kPacked>(p.lq, bh, h, sq.start, row, D);
+            // O in 32-column chunks, the next chunk's TMEM load overlapping this
+            // chunk's conversion and stores
+            uint32_t ob[2][32];
+            if (ntile > 0) {
+                tmem_ld32(t_O, ob[0]);
+                tmem_ld_wait();
+                reg_fence(ob[0]);
+            }
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                if (ntile > 0) {
-                    tmem_ld32(t_O + 32 * c, o);
-                    tmem_ld_wait();
-                    reg_fence(o);
-                } else {
+                if (ntile > 0 && c + 1 < D / 32) tmem_ld32(t_O + 32 * (c + 1), ob[(c + 1) & 1]);
+                uint32_t* o = ob[c & 1];
+                if (ntile == 0) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = 0u;
                 }
@@ -626,6 +631,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
                             dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     }
+                }
+                if (ntile > 0 && c + 1 < D / 32) {
+                    tmem_ld_wait();
+                    reg_fence(ob[(c + 1) & 1]);
                 }
             }
             if (row < N)
