@@ -11,8 +11,11 @@ unsupported, the call raises.
     dq, dk, dv = ea.attn_bwd(q, k, v, o, do, lse, causal=True)
 
 q, o, do, dq are [B, H, N, d] and k, v, dk, dv [B, H, Nk, d] (Nk = N for
-self-attention), contiguous, on one CUDA device; bf16 or fp16 (d = 64 or 128)
-or, forward only, fp32 with d = 64.
+self-attention), contiguous, on one CUDA device; bf16 or fp16 (d = 64 or 128;
+the forward also d = 256), or, forward only, fp32 with d = 64 and e4m3
+(torch.float8_e4m3fn, O in bf16) with d = 128.  attn_fwd_varlen and
+attn_bwd_varlen take packed sequences: [total, H, d] tensors and cumulative
+offsets.
 """
 from __future__ import annotations
 

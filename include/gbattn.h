@@ -129,8 +129,9 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d);
 /*
  * Backward pass: given the forward's inputs, its O and LSE and the incoming
  * gradient dO, writes dQ ([B, H, N, d]) and dK, dV ([B, H, Nk, d]), in the
- * dtype of Q.  bf16 or fp16, d in {64, 128}.  workspace must hold attn_bwd_workspace_size(B, H, N, d)
- * bytes (16-byte aligned); its contents on entry do not matter.  Enqueues
+ * dtype of Q.  bf16 or fp16, d in {64, 128}.  workspace must hold
+ * attn_bwd_workspace_size(B, H, N, d) bytes (16-byte aligned); its contents
+ * on entry do not matter.  Enqueues
  * three launches: attn_bwd_preprocess, attn_bwd_main, attn_bwd_dq_convert.
  */
 attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
