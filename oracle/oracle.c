@@ -35,7 +35,7 @@
  *     easy as 1, 2, 3", SC'11), written from the paper's definition, used for
  *     the dropout keep/drop decision.
  *
- * Readings of points the pages leave open (each also listed in the design doc):
+ * Readings of points the pages leave open:
  *   - mask: key j of sequence b is valid iff j < key_len[b] and, when causal,
  *     j <= i, and, when window w > 0 (sliding-window attention, named as a
  *     variant in "Why FlashAttention Is a Kernel Story", "When it falls down"),
