@@ -197,3 +197,30 @@ def test_product_code_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "liboracle" not in text and "oracle.c" not in text, f
+
+
+def test_binding_rejects_bad_packed_arguments_before_any_call():
+    """The Python binding checks packed-sequence tensors before it reaches the
+    library (CPU tensors: any call into the library would fail differently)."""
+    import torch
+    q = torch.zeros(10, 2, 64, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 4, 10], dtype=torch.int32)
+    with pytest.raises(ValueError, match="k must be"):
+        ea.attn_fwd_varlen(q, torch.zeros(10, 3, 64, dtype=torch.bfloat16), q, cu, cu, 6, 6)
+    with pytest.raises(ValueError, match="v must match"):
+        ea.attn_fwd_varlen(q, q, torch.zeros(9, 2, 64, dtype=torch.bfloat16), cu, cu, 6, 6)
+    with pytest.raises(ValueError, match="cu_seqlens_q"):
+        ea.attn_fwd_varlen(q, q, q, cu.to(torch.int64), cu, 6, 6)
+    with pytest.raises(ValueError, match="same length"):
+        ea.attn_fwd_varlen(q, q, q, cu, torch.tensor([0, 10], dtype=torch.int32), 6, 6)
+    with pytest.raises(ValueError, match="expected q"):
+        ea.attn_fwd_varlen(q[None], q, q, cu, cu, 6, 6)
+
+
+def test_binding_rejects_mismatched_dense_keys():
+    import torch
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="k must be"):
+        ea.attn_fwd(q, torch.zeros(1, 3, 8, 64, dtype=torch.bfloat16), q)
+    with pytest.raises(ValueError, match="k must be"):
+        ea.attn_fwd(q, torch.zeros(1, 2, 8, 32, dtype=torch.bfloat16), q)
