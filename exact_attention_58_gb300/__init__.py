@@ -32,7 +32,7 @@ from . import _build
 __all__ = [
     "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
     "attn_bwd_main", "attn_bwd_dq_convert", "attn_bwd_noalloc", "attn_fwd_varlen",
-    "attn_bwd_varlen", "attn_status_string", "attn_version", "library",
+    "attn_bwd_varlen", "attn_selftest_wait", "attn_status_string", "attn_version", "library",
     "LIB_PATH", "STATUS",
 ]
 
@@ -91,6 +91,8 @@ def library():
                                                               vp]
             lib.attn_bwd_dq_convert.argtypes = [vp, ip, ip, ip, ip, ip, f, vp, sz, vp]
             lib.attn_fwd_varlen.argtypes = [vp] * 7 + [ip] * 8 + [f, ip, ip, f, u64, vp, vp]
+            lib.attn_selftest_wait.argtypes = [vp, ip, vp]
+            lib.attn_selftest_wait.restype = ctypes.c_int
             lib.attn_bwd_varlen.argtypes = ([vp] * 11 + [ip] * 8 +
                                             [f, ip, ip, f, u64, vp, sz, vp, vp])
             for fn in ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
@@ -396,3 +398,11 @@ def attn_bwd_varlen(q, k, v, o, do, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_
                                    _ptr(dev_status), _stream(stream))
     _raise(st, "attn_bwd_varlen")
     return dq, dk, dv
+
+
+def attn_selftest_wait(dev_status, *, arrive: bool, stream=None):
+    """Device self-test of the bounded waits (see include/gbattn.h): with
+    arrive=False the wait expires and ATTN_ERR_DEVICE_TIMEOUT lands in
+    dev_status (a CUDA int32 tensor, 0 on entry)."""
+    st = library().attn_selftest_wait(_ptr(dev_status), int(bool(arrive)), _stream(stream))
+    _raise(st, "attn_selftest_wait")

@@ -224,6 +224,17 @@ attn_status attn_bwd_varlen(const void* Q, const void* K, const void* V, const v
                             int window, float dropout_p, uint64_t seed, void* workspace,
                             size_t workspace_bytes, int* dev_status, void* stream);
 
+/*
+ * Device self-test of the failure detection the kernels rely on: one warp
+ * waits on an mbarrier with the same bounded wait (about 2 s of
+ * %globaltimer) that every kernel uses.  arrive != 0: one thread arrives
+ * first, the wait succeeds and *dev_status is left as it is.  arrive == 0:
+ * nothing arrives, the wait expires and ATTN_ERR_DEVICE_TIMEOUT is written to
+ * *dev_status (a device int, 0 on entry).  Nothing else is in flight, so the
+ * expiry leaves the context usable.  Not part of the attention path.
+ */
+attn_status attn_selftest_wait(int* dev_status, int arrive, void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* attn_status_string(attn_status status);
 
