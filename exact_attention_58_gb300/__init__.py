@@ -135,22 +135,62 @@ def _stream(stream) -> ctypes.c_void_p:
 
 
 def _shape(q: torch.Tensor):
-    if q.dim() != 4:
+    if not isinstance(q, torch.Tensor) or q.dim() != 4:
         raise ValueError("expected a [B, H, N, d] tensor")
+    _check_like("q", q, q)
     return tuple(int(x) for x in q.shape)
 
 
 def _check_like(name: str, t: torch.Tensor, ref: torch.Tensor):
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a tensor")
     if t.shape != ref.shape or t.dtype != ref.dtype or t.device != ref.device:
         raise ValueError(f"{name} must match q in shape, dtype and device")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
 
 
+def _on_gpu(q: torch.Tensor):
+    """Every tensor argument has been checked to be on q's device; that device
+    must be a CUDA one (a host pointer handed to a kernel would be read or
+    written as if it were device memory)."""
+    if not q.is_cuda:
+        raise ValueError("the tensors must be on a CUDA device")
+
+
+def _check_lse(lse, shape, q: torch.Tensor):
+    """The log-sum-exp buffer: contiguous float32 of `shape` on q's device."""
+    if (not isinstance(lse, torch.Tensor) or lse.dtype != torch.float32
+            or tuple(lse.shape) != tuple(shape) or lse.device != q.device
+            or not lse.is_contiguous()):
+        raise ValueError(f"lse must be a contiguous float32 tensor of shape {tuple(shape)} "
+                         "on q's device")
+    return lse
+
+
+def _check_status(dev_status, q: torch.Tensor):
+    """dev_status: None, or an int32 tensor (at least one element) on q's device."""
+    if dev_status is None:
+        return None
+    if (not isinstance(dev_status, torch.Tensor) or dev_status.dtype != torch.int32
+            or dev_status.numel() < 1 or dev_status.device != q.device
+            or not dev_status.is_contiguous()):
+        raise ValueError("dev_status must be a contiguous int32 tensor with at least one "
+                         "element on q's device")
+    return dev_status
+
+
+def _check_workspace(workspace, q: torch.Tensor):
+    if (not isinstance(workspace, torch.Tensor) or workspace.device != q.device
+            or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous tensor on q's device")
+    return workspace
+
+
 def _keys(q: torch.Tensor, k: torch.Tensor) -> int:
     """Nk of k, which must be [B, H, Nk, d] like q apart from its length."""
-    if (k.dim() != 4 or k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]
-            or k.dtype != q.dtype or k.device != q.device):
+    if (not isinstance(k, torch.Tensor) or k.dim() != 4 or k.shape[:2] != q.shape[:2]
+            or k.shape[3] != q.shape[3] or k.dtype != q.dtype or k.device != q.device):
         raise ValueError("k must be [B, H, Nk, d] with q's B, H, d, dtype and device")
     if not k.is_contiguous():
         raise ValueError("k must be contiguous")
@@ -198,7 +238,10 @@ def attn_fwd(q, k, v, *, causal: bool = False, window: int = 0, key_lens=None,
         raise ValueError("out must be a contiguous tensor of q's shape (bf16 for e4m3 q)")
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_lse(lse, (B, H, N), q)
+    _check_status(dev_status, q)
     kl = _key_lens(key_lens, q)
+    _on_gpu(q)
     st = library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, Nk, d,
                             _dtype_code(q), float(scale), int(bool(causal)), int(window), _ptr(kl),
                             float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(dev_status),
@@ -207,10 +250,11 @@ def attn_fwd(q, k, v, *, causal: bool = False, window: int = 0, key_lens=None,
     return out, lse
 
 
-def _workspace(B, H, N, d, workspace, device):
+def _workspace(B, H, N, d, workspace, q):
     need = attn_bwd_workspace_size(B, H, N, d)
     if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check_workspace(workspace, q)
     return workspace, int(workspace.numel() * workspace.element_size())
 
 
@@ -231,8 +275,11 @@ def attn_bwd(q, k, v, o, do, lse, *, causal: bool = False, window: int = 0, key_
     _check_like("dq", dq, q)
     _check_like("dk", dk, k)
     _check_like("dv", dv, k)
-    ws, ws_bytes = _workspace(B, H, N, d, workspace, q.device)
+    _check_lse(lse, (B, H, N), q)
+    _check_status(dev_status, q)
+    ws, ws_bytes = _workspace(B, H, N, d, workspace, q)
     kl = _key_lens(key_lens, q)
+    _on_gpu(q)
     st = library().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
                             _ptr(dk), _ptr(dv), B, H, N, Nk, d, _dtype_code(q), float(scale),
                             int(bool(causal)), int(window), _ptr(kl), float(dropout_p),
@@ -262,7 +309,10 @@ def attn_bwd_noalloc(q, k, v, o, do, lse, *, causal: bool = False, window: int =
     _check_like("dq", dq, q)
     _check_like("dk", dk, k)
     _check_like("dv", dv, k)
+    _check_lse(lse, (B, H, N), q)
+    _check_status(dev_status, q)
     kl = _key_lens(key_lens, q)
+    _on_gpu(q)
     st = library().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
                                     _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, Nk, d, _dtype_code(q),
                                     float(scale), int(bool(causal)), int(window), _ptr(kl),
@@ -276,6 +326,9 @@ def attn_bwd_noalloc(q, k, v, o, do, lse, *, causal: bool = False, window: int =
 def attn_bwd_preprocess(o, do, lse, workspace, *, stream=None):
     B, H, N, d = _shape(o)
     _check_like("do", do, o)
+    _check_lse(lse, (B, H, N), o)
+    _check_workspace(workspace, o)
+    _on_gpu(o)
     st = library().attn_bwd_preprocess(_ptr(o), _ptr(do), _ptr(lse), B, H, N, d,
                                        _dtype_code(o), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(),
@@ -287,9 +340,16 @@ def attn_bwd_main(q, k, v, do, dk, dv, workspace, *, causal=False, window=0, key
                   dropout_p=0.0, seed=0, scale=None, dev_status=None, stream=None):
     B, H, N, d = _shape(q)
     Nk = _keys(q, k)
+    _check_like("v", v, k)
+    _check_like("do", do, q)
+    _check_like("dk", dk, k)
+    _check_like("dv", dv, k)
+    _check_workspace(workspace, q)
+    _check_status(dev_status, q)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     kl = _key_lens(key_lens, q)
+    _on_gpu(q)
     st = library().attn_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dk), _ptr(dv), B, H,
                                  N, Nk, d, _dtype_code(q), float(scale), int(bool(causal)),
                                  int(window), _ptr(kl),
@@ -301,8 +361,10 @@ def attn_bwd_main(q, k, v, do, dk, dv, workspace, *, causal=False, window=0, key
 
 def attn_bwd_dq_convert(dq, workspace, *, scale=None, stream=None):
     B, H, N, d = _shape(dq)
+    _check_workspace(workspace, dq)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    _on_gpu(dq)
     st = library().attn_bwd_dq_convert(_ptr(dq), B, H, N, d, _dtype_code(dq), float(scale),
                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
                                        _stream(stream))
@@ -313,6 +375,8 @@ def attn_bwd_dq_convert(dq, workspace, *, scale=None, stream=None):
 # packed variable-length sequences
 # ---------------------------------------------------------------------------
 def _packed(name: str, t: torch.Tensor, H: int, d: int, ref: torch.Tensor):
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a tensor")
     if (t.dim() != 3 or t.shape[1] != H or t.shape[2] != d or t.dtype != ref.dtype
             or t.device != ref.device):
         raise ValueError(f"{name} must be [total, H, d] with q's H, d, dtype and device")
@@ -354,6 +418,9 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_
         raise ValueError("out must be a contiguous tensor of q's shape (bf16 for e4m3 q)")
     if lse is None:
         lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    _check_lse(lse, (H, total_q), q)
+    _check_status(dev_status, q)
+    _on_gpu(q)
     st = library().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
                                    _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, H, total_q, total_k,
                                    int(max_seqlen_q), int(max_seqlen_k), d, _dtype_code(q),
@@ -372,6 +439,7 @@ def attn_bwd_varlen(q, k, v, o, do, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_
     if q.dim() != 3:
         raise ValueError("expected q as [total_q, H, d]")
     total_q, H, d = (int(x) for x in q.shape)
+    _packed("q", q, H, d, q)
     total_k = _packed("k", k, H, d, q)
     if _packed("v", v, H, d, q) != total_k:
         raise ValueError("v must match k")
@@ -388,7 +456,10 @@ def attn_bwd_varlen(q, k, v, o, do, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_
     _check_like("dq", dq, q)
     _check_like("dk", dk, k)
     _check_like("dv", dv, k)
-    ws, ws_bytes = _workspace(B, H, int(max_seqlen_q), d, workspace, q.device)
+    _check_lse(lse, (H, total_q), q)
+    _check_status(dev_status, q)
+    ws, ws_bytes = _workspace(B, H, int(max_seqlen_q), d, workspace, q)
+    _on_gpu(q)
     st = library().attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q),
                                    _ptr(cu_seqlens_k), B, H, total_q, total_k, int(max_seqlen_q),

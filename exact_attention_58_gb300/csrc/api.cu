@@ -284,6 +284,22 @@ attn_status bwd_impl(const void* Q, const void* K, const void* V, const void* O,
 SeqLayout dense(int H, int N) { return SeqLayout{nullptr, H, N, 0}; }
 
 }  // namespace
+
+attn_status check_bwd_args(const void* Q, const void* K, const void* V, const void* O,
+                           const void* dO, const float* LSE, const void* dQ, const void* dK,
+                           const void* dV, int B, int H, int N, int Nk, int d, attn_dtype dtype,
+                           float scale, float dropout_p) {
+    if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
+    attn_status st = check_shape(B, H, N, d, dtype, true);
+    if (st != ATTN_OK) return st;
+    if ((st = check_keys(B, H, Nk, d)) != ATTN_OK) return st;
+    if ((st = check_math(scale, dropout_p)) != ATTN_OK) return st;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) ||
+        !aligned16(LSE) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
+        return ATTN_ERR_MISALIGNED;
+    return ATTN_OK;
+}
+
 }  // namespace gbattn
 
 using namespace gbattn;
@@ -361,10 +377,9 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
                      int d, attn_dtype dtype, float scale, int causal, int window,
                      const int32_t* key_lens, float dropout_p, uint64_t seed, void* workspace,
                      size_t workspace_bytes, int* dev_status, void* stream) {
-    if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
-    attn_status st = check_shape(B, H, N, d, dtype, true);
+    const attn_status st = check_bwd_args(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, Nk, d, dtype,
+                                          scale, dropout_p);
     if (st != ATTN_OK) return st;
-    if ((st = check_keys(B, H, Nk, d)) != ATTN_OK) return st;
     return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, dense(H, N), dense(H, Nk), d, dtype, scale,
                     causal, window, key_lens, dropout_p, seed, workspace, workspace_bytes,
                     dev_status, stream);

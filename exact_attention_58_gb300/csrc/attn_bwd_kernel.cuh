@@ -677,12 +677,9 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
                          const BwdParams& p, cudaStream_t stream) {
     using C = BwdCfg<D, kF16>;
     auto kern = attn_bwd_kernel<D, kF16, kCausal, kDropout, kWindow, kPacked>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<unsigned long long> smem_ready{0};
+    const cudaError_t e = enable_smem_per_device(kern, C::SMEM, smem_ready);
+    if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(p.nkb) * static_cast<unsigned>(p.B * p.H);
     kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdk, tdv, p);
     return cudaGetLastError();

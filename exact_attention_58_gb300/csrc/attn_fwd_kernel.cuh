@@ -658,12 +658,9 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
                          const FwdParams& p, cudaStream_t stream) {
     using C = FwdCfg<D, kTF32, kF16, kFP8>;
     auto kern = attn_fwd_kernel<D, kTF32, kF16, kFP8, kCausal, kDropout, kWindow, kPacked>;
-    static bool configured = false;   // benign race: the attribute call is idempotent
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<unsigned long long> smem_ready{0};
+    const cudaError_t e = enable_smem_per_device(kern, C::SMEM, smem_ready);
+    if (e != cudaSuccess) return e;
     FwdParams pp = p;
     pp.nqb = (p.N + kTileRows * C::TILES - 1) / (kTileRows * C::TILES);
     const unsigned grid = static_cast<unsigned>(pp.nqb) * static_cast<unsigned>(p.B * p.H);

@@ -3,6 +3,8 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <cstdint>
 
 #include "gbattn.h"
@@ -62,12 +64,37 @@ struct BwdParams {
     SeqLayout lq, lk;         // query / key row placement (N, Nk are their N)
 };
 
+// Dynamic shared memory above 48 KB has to be enabled for a kernel in each
+// device's context before its first launch there.  `done` (one per kernel)
+// remembers the devices already set up; the attribute call is idempotent, so
+// two threads that race on the first launch both succeed.  Devices past the
+// 64 bits of the mask set the attribute on every launch.
+template <typename Kernel>
+cudaError_t enable_smem_per_device(Kernel kern, int bytes, std::atomic<unsigned long long>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
 // Tensor map over a contiguous [B*H][N][d] array, 128-row boxes of 128 bytes
 // along d, 128-byte swizzle.  Returns false if the driver rejected it.
 bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int BH, int N, int d);
 // Tensor map over a contiguous [T][H][d] array (packed sequences) with the
 // same boxes: 128 consecutive tokens of one head, 128 bytes along d.
 bool make_tmap_thd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int T, int H, int d);
+
+// Every check attn_bwd makes before it looks at the workspace: NULL pointers,
+// shape, key count, scale, dropout probability and 16-byte alignment, in that
+// order, with attn_bwd's status codes.
+attn_status check_bwd_args(const void* Q, const void* K, const void* V, const void* O,
+                           const void* dO, const float* LSE, const void* dQ, const void* dK,
+                           const void* dV, int B, int H, int N, int Nk, int d, attn_dtype dtype,
+                           float scale, float dropout_p);
 
 // Forward launch (validated arguments only).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

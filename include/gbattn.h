@@ -74,6 +74,12 @@
  *             int, 0 = OK) when dev_status is not NULL; the kernel then exits
  *             cleanly and leaves the affected outputs unspecified.
  *  Threads    Every entry point is thread-safe.
+ *  Devices    One process may drive several GPUs: every call runs on the
+ *             device current in the calling thread (cudaSetDevice), whose
+ *             context gets its own one-time kernel set-up on first use, and
+ *             all pointers of a call must be memory of that device.  The library must not outlive a reset of
+ *             a device it has used (cudaDeviceReset): what it set up in the
+ *             old context is not redone in the new one.
  */
 #ifndef GBATTN_H
 #define GBATTN_H
@@ -175,12 +181,15 @@ attn_status attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, attn_dtype
  *             rejected with ATTN_ERR_WORKSPACE before anything is enqueued.
  *   Set-up    the first call on a device looks up the buffer's device address
  *             (cudaGetSymbolAddress) with that device current; make that first
- *             call before any stream capture.
+ *             call before any stream capture.  The address is looked up again
+ *             if the device's context has changed since (a device reset).
  *   Sharing   every call uses the same buffer; each call clears what must
  *             start at zero, but calls that overlap on the GPU race on it.
  *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  * Otherwise identical to attn_bwd (same arguments minus the workspace, same
- * results, same errors).
+ * results, same errors).  attn_bwd's argument errors are checked first; a
+ * shape that passes them but needs more scratch than 32 MiB then returns
+ * ATTN_ERR_WORKSPACE.
  */
 attn_status attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
                              const void* dO, const float* LSE, void* dQ, void* dK, void* dV,

@@ -9,8 +9,13 @@ import exact_attention_58_gb300 as ea
 import oracle
 
 # Tolerances.  O: max |O - O_ref| <= 2e-2 (bf16 inputs, fp32 accumulation).
-# LSE: l sums bf16-rounded probabilities (relative error <= 2^-9 per term), so
-# |LSE - LSE_ref| <= 2^-9 plus fp32 rounding; 4e-3 leaves a factor of two.
+# LSE = ln 2 (m + log2 l): the row max m comes from fp32 scores, each the fp32
+# sum of d exact products of 16-bit (or e4m3) inputs (absolute error about
+# d 2^-24 sum_k |q_k k_k| scale log2e, below 1e-4 for unit-variance inputs at
+# d <= 256); l is the fp32 sum of the unrounded exp2 values (ex2.approx, about
+# 2^-22 relative each) over at most N keys, at most N 2^-24 relative (2.4e-4
+# at N = 4096), which moves LSE by the same amount.  The budget is a few 1e-4;
+# 4e-3 is the tolerance, with a margin of ten.
 # Gradients: max |g - g_ref| / max |g_ref| <= 5e-2 per tensor.
 O_ATOL = 2e-2
 LSE_ATOL = 4e-3

@@ -224,3 +224,65 @@ def test_binding_rejects_mismatched_dense_keys():
         ea.attn_fwd(q, torch.zeros(1, 3, 8, 64, dtype=torch.bfloat16), q)
     with pytest.raises(ValueError, match="k must be"):
         ea.attn_fwd(q, torch.zeros(1, 2, 8, 32, dtype=torch.bfloat16), q)
+
+
+def _noalloc(lib, **kw):
+    a = dict(B=4, H=16, N=4096, d=128, dtype=0, scale=0.088, p=0.0, ptrs=[FAKE] * 9)
+    a.update(kw)
+    a.setdefault("Nk", a["N"])
+    return lib.attn_bwd_noalloc(*a["ptrs"], a["B"], a["H"], a["N"], a["Nk"], a["d"], a["dtype"],
+                                a["scale"], 1, 0, None, a["p"], 0, None, None)
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(), 4),                                   # valid, but 136 MB of scratch > 32 MiB
+    (dict(dtype=1), 2),                            # fp32 backward: unsupported, whatever the size
+    (dict(scale=float("nan")), 1),
+    (dict(p=1.0), 1),
+    (dict(Nk=0), 1),
+    (dict(ptrs=[FAKE] * 8 + [FAKE + 8]), 3),      # misaligned dV
+    (dict(ptrs=[FAKE] * 8 + [None]), 1),
+])
+def test_noalloc_reports_attn_bwd_errors_before_its_size_limit(lib, kw, expected):
+    """attn_bwd_noalloc returns the same argument errors as attn_bwd; only a
+    shape that passes them and needs more than the built-in scratch gets
+    ATTN_ERR_WORKSPACE."""
+    assert _noalloc(lib, **kw) == expected
+
+
+def test_binding_rejects_views_and_foreign_buffers():
+    """Malformed tensors are refused by the binding before the library sees
+    them: a transposed (non-contiguous) q, an lse of the wrong type or shape,
+    a dev_status that is not int32, and tensors that are not on a GPU."""
+    import torch
+    B, H, N, d = 1, 2, 8, 64
+    x = torch.zeros(B, H, N, d, dtype=torch.bfloat16)
+    qt = torch.zeros(B, N, H, d, dtype=torch.bfloat16).transpose(1, 2)   # [B, H, N, d] view
+    lse = torch.zeros(B, H, N, dtype=torch.float32)
+    with pytest.raises(ValueError, match="q must be contiguous"):
+        ea.attn_bwd(qt, x, x, x, x, lse)
+    with pytest.raises(ValueError, match="q must be contiguous"):
+        ea.attn_bwd_noalloc(qt, x, x, x, x, lse)
+    with pytest.raises(ValueError, match="q must be contiguous"):
+        ea.attn_fwd(qt, x, x)
+    with pytest.raises(ValueError, match="lse must be"):
+        ea.attn_bwd(x, x, x, x, x, lse.to(torch.float16))
+    with pytest.raises(ValueError, match="lse must be"):
+        ea.attn_bwd(x, x, x, x, x, lse[:, :, :4])
+    with pytest.raises(ValueError, match="lse must be"):
+        ea.attn_fwd(x, x, x, lse=lse.double())
+    with pytest.raises(ValueError, match="dev_status must be"):
+        ea.attn_fwd(x, x, x, dev_status=torch.zeros(1, dtype=torch.int64))
+    with pytest.raises(ValueError, match="dev_status must be"):
+        ea.attn_bwd(x, x, x, x, x, lse, dev_status=torch.zeros(0, dtype=torch.int32))
+    with pytest.raises(ValueError, match="CUDA device"):
+        ea.attn_fwd(x, x, x)
+    with pytest.raises(ValueError, match="CUDA device"):
+        ea.attn_bwd(x, x, x, x, x, lse, workspace=torch.zeros(1 << 16, dtype=torch.uint8))
+    pq = torch.zeros(10, H, d, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 4, 10], dtype=torch.int32)
+    with pytest.raises(ValueError, match="q must be"):
+        ea.attn_bwd_varlen(torch.zeros(10, d, H, dtype=torch.bfloat16).transpose(1, 2), pq, pq,
+                           pq, pq, torch.zeros(H, 10), cu, cu, 6, 6)
+    with pytest.raises(ValueError, match="lse must be"):
+        ea.attn_bwd_varlen(pq, pq, pq, pq, pq, torch.zeros(H, 9), cu, cu, 6, 6)

@@ -43,10 +43,18 @@ def test_noalloc_matches_workspace_backward_twice(d, causal):
     ref = ea.attn_bwd(q, k, v, o, do, lse, causal=causal, key_lens=kl,
                       dropout_p=inp.dropout_p, seed=inp.seed, scale=inp.scale)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = [tuple(torch.full_like(q, float("nan")) for _ in range(3)) for _ in range(2)]
+    torch.cuda.synchronize()
     for call in range(2):   # the buffer keeps the last call's contents: both must be right
-        dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+        dq, dk, dv = outs[call]
+        if call == 1:   # device memory in use, seen by the driver and by torch's allocator
+            free0, _ = torch.cuda.mem_get_info()
+            alloc0 = torch.cuda.memory_allocated()
         st = _call_noalloc(lib, q, k, v, o, do, lse, dq, dk, dv, inp, status)
         torch.cuda.synchronize()
+        if call == 1:   # the call itself allocated nothing (kernels were loaded by call 0)
+            assert torch.cuda.mem_get_info()[0] == free0
+            assert torch.cuda.memory_allocated() == alloc0
         assert st == 0, ea.attn_status_string(st)
         assert int(status.item()) == 0
         for got, want, name in zip((dq, dk, dv), ref, ("dQ", "dK", "dV")):
