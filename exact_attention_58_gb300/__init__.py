@@ -32,7 +32,8 @@ from . import _build
 __all__ = [
     "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess",
     "attn_bwd_main", "attn_bwd_dq_convert", "attn_bwd_noalloc", "attn_fwd_varlen",
-    "attn_bwd_varlen", "attn_selftest_wait", "attn_status_string", "attn_version", "library",
+    "attn_bwd_varlen", "attn_selftest_wait", "attn_selftest_fwd_withheld", "attn_status_string",
+    "attn_version", "library",
     "LIB_PATH", "STATUS",
 ]
 
@@ -93,6 +94,8 @@ def library():
             lib.attn_fwd_varlen.argtypes = [vp] * 7 + [ip] * 8 + [f, ip, ip, f, u64, vp, vp]
             lib.attn_selftest_wait.argtypes = [vp, ip, vp]
             lib.attn_selftest_wait.restype = ctypes.c_int
+            lib.attn_selftest_fwd_withheld.argtypes = [vp] * 5 + [ip] * 6 + [vp, vp]
+            lib.attn_selftest_fwd_withheld.restype = ctypes.c_int
             lib.attn_bwd_varlen.argtypes = ([vp] * 11 + [ip] * 8 +
                                             [f, ip, ip, f, u64, vp, sz, vp, vp])
             for fn in ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
@@ -477,3 +480,29 @@ def attn_selftest_wait(dev_status, *, arrive: bool, stream=None):
     dev_status (a CUDA int32 tensor, 0 on entry)."""
     st = library().attn_selftest_wait(_ptr(dev_status), int(bool(arrive)), _stream(stream))
     _raise(st, "attn_selftest_wait")
+
+
+def attn_selftest_fwd_withheld(q, k, v, dev_status, *, withhold_block: int, wait_ms: int = 20,
+                               out=None, lse=None, stream=None):
+    """Device self-test of the forward kernel's abort path (see
+    include/gbattn.h): bf16 [B, H, N, 128] q and [B, H, Nk, 128] k, v; the K
+    tile of key block `withhold_block` is never loaded (< 0: nothing withheld)
+    and waits give up after `wait_ms`.  dev_status: a CUDA int32 tensor, 0 on
+    entry."""
+    B, H, N, d = _shape(q)
+    Nk = _keys(q, k)
+    _check_like("v", v, k)
+    if q.dtype != torch.bfloat16 or d != 128:
+        raise ValueError("the self test runs bf16 with d = 128")
+    out = torch.empty_like(q) if out is None else out
+    _check_like("out", out, q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_lse(lse, (B, H, N), q)
+    if _check_status(dev_status, q) is None:
+        raise ValueError("dev_status is required")
+    _on_gpu(q)
+    st = library().attn_selftest_fwd_withheld(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B,
+                                              H, N, Nk, int(withhold_block), int(wait_ms),
+                                              _ptr(dev_status), _stream(stream))
+    _raise(st, "attn_selftest_fwd_withheld")
+    return out, lse

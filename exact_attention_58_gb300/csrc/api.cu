@@ -5,6 +5,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 #include "internal.h"
@@ -116,6 +117,18 @@ bool encode_3d(CUtensorMap* map, const void* ptr, attn_dtype dtype, const cuuint
 
 }  // namespace
 
+int fwd_tiles(int d, attn_dtype dtype, int N) {
+    if (d > 128) return 1;
+    if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP16) return 2;
+    const char* env = std::getenv("GBATTN_FWD_TILES");
+    if (env != nullptr && (env[0] == '1' || env[0] == '2') && env[1] == '\0') return env[0] - '0';
+    // Measured on GB300: at d = 64 with short sequences (N = 512, 1024) one
+    // tile per CTA is as fast or faster (more, shorter CTAs balance better and
+    // two CTAs per SM overlap one's start-up with the other's work); with
+    // long sequences or d = 128 two tiles sharing each K/V block win.
+    return (d == 64 && N <= 2048) ? 1 : 2;
+}
+
 bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int BH, int N, int d) {
     const cuuint64_t es = elem_bytes(dtype);
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
@@ -196,7 +209,7 @@ attn_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float
     p.lq = lq;
     p.lk = lk;
     return from_cuda(launch_fwd(tq, tk, tv, p, d, dtype, causal != 0, dropout_p > 0.f,
-                                static_cast<cudaStream_t>(stream)));
+                                fwd_tiles(d, dtype, lq.N), static_cast<cudaStream_t>(stream)));
 }
 
 attn_status pre_impl(const void* O, const void* dO, const float* LSE, int B, const SeqLayout& lq,

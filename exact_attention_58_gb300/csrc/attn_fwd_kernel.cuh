@@ -47,7 +47,7 @@
 namespace gbattn {
 namespace {
 
-template <int D, bool kTF32, bool kF16, bool kFP8>
+template <int D, bool kTF32, bool kF16, bool kFP8, int kTiles>
 struct FwdCfg {
     static constexpr int ES = kTF32 ? 4 : (kFP8 ? 1 : 2);  // element bytes of Q, K, V
     static constexpr int ROWB = D * ES;                    // bytes per row
@@ -58,7 +58,8 @@ struct FwdCfg {
     // Query tiles per CTA: two tiles share each K/V block in one CTA, or one
     // tile per CTA with two CTAs resident on an SM.  d = 256 takes one tile:
     // its O accumulator alone fills half of tensor memory.
-    static constexpr int TILES = D == 256 ? 1 : kFwdTilesPerCta;
+    static constexpr int TILES = kTiles;
+    static_assert(kTiles == 1 || (kTiles == 2 && D <= 128), "two tiles fit tensor memory up to d = 128");
     static constexpr int NSLOT = (TILES == 2 ? 4 : 2) * ((ROWB == 128) ? 2 : 1);   // K/V ring slots
     static constexpr int THREADS = 32 * (4 * TILES + 2);   // softmax warps, producer, MMA
     static constexpr int PRODUCER_WARP = 4 * TILES;
@@ -107,14 +108,18 @@ __device__ __forceinline__ void store_v_transposed(const float* __restrict__ Vh,
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
+// kSelfTest (one test instantiation only, never the attn_fwd path): the
+// producer withholds the K tile of key block p.withhold_block and every wait
+// gives up after p.wait_ns, so that a wait expires with copies and products
+// in flight and the abort path below runs on the GPU.
 template <int D, bool kTF32, bool kF16, bool kFP8, bool kCausal, bool kDropout, bool kWindow,
-          bool kPacked>
-__global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
-                                  FwdCfg<D, kTF32, kF16, kFP8>::CTAS_PER_SM)
+          bool kPacked, int kTiles, bool kSelfTest = false>
+__global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8, kTiles>::THREADS,
+                                  FwdCfg<D, kTF32, kF16, kFP8, kTiles>::CTAS_PER_SM)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-    using C = FwdCfg<D, kTF32, kF16, kFP8>;
+    using C = FwdCfg<D, kTF32, kF16, kFP8, kTiles>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -133,6 +138,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const unsigned long long lim = kSelfTest ? p.wait_ns : kWaitLimitNs;
 
     // ---- which 256 query rows of which head ----
     const int BH = p.B * p.H;
@@ -237,14 +243,19 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
                 }
             }
             int seq = 0;
+            int withheld = -1;   // the fill left out (self test only)
             bool ok = true;
             for (int j = jbeg; j < jbeg + nkv && ok; ++j) {
                 for (int which = 0; which < 2; ++which) {
                     const int slot = seq % C::NSLOT;
                     const uint32_t ph = (seq / C::NSLOT) & 1;
-                    if (!mbar_wait_warp(&empty[slot], ph ^ 1, s_abort)) {
+                    if (!mbar_wait_warp(&empty[slot], ph ^ 1, s_abort, lim)) {
                         ok = false;
                         break;
+                    }
+                    if (kSelfTest && which == 0 && j == p.withhold_block) {   // no copy, no arrival
+                        withheld = seq++;
+                        continue;
                     }
                     if (kTF32 && which == 1) {
                         store_v_transposed<D>(static_cast<const float*>(p.V) +
@@ -268,10 +279,13 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
             // Drain: every load this warp issued has landed before teardown.
             if (lane == 0) {
                 volatile int no_abort = 0;
-                mbar_wait(bar_q, 0, &no_abort);
+                mbar_wait(bar_q, 0, &no_abort, lim);
                 for (int s = 0; s < C::NSLOT && s < seq; ++s) {
                     const int uses = (seq - s + C::NSLOT - 1) / C::NSLOT;
-                    mbar_wait(&full[s], (uses - 1) & 1, &no_abort);
+                    // a withheld fill is always its slot's last: nothing refills
+                    // a slot whose consumer never got its tile
+                    if (s + (uses - 1) * C::NSLOT == withheld) continue;
+                    mbar_wait(&full[s], (uses - 1) & 1, &no_abort, lim);
                 }
             }
         }
@@ -316,7 +330,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
                                       (accumulate || kk > 0) ? 1u : 0u);
                 }
             };
-            bool ok = mbar_wait(bar_q, 0, s_abort);
+            bool ok = mbar_wait(bar_q, 0, s_abort, lim);
             tc_fence_after();
             int seq = 0;
             int v_slot = 0;
@@ -335,11 +349,11 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
                     const bool prev = j - 1 >= jlo(t) && j - 1 < jhi(t);   // tile t saw block j-1
                     const bool last_pv = prev && j == jhi(t);
                     if (prev) {   // O_t += P_t(j-1) V_{j-1}, once the softmax of j-1 is done
-                        ok = mbar_wait(&bar_p[t], (j - 1 - jlo(t)) & 1, s_abort);
+                        ok = mbar_wait(&bar_p[t], (j - 1 - jlo(t)) & 1, s_abort, lim);
                         if (!ok) break;
                         tc_fence_after();
                         if (!v_ready) {
-                            ok = mbar_wait(&full[v_slot], v_phase, s_abort);
+                            ok = mbar_wait(&full[v_slot], v_phase, s_abort, lim);
                             v_ready = true;
                             if (!ok) break;
                             tc_fence_after();
@@ -349,7 +363,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
                     }
                     if (qk) {                         // S_t = Q_t K_j^T
                         if (!k_ready) {
-                            ok = mbar_wait(&full[kslot], kph, s_abort);
+                            ok = mbar_wait(&full[kslot], kph, s_abort, lim);
                             k_ready = true;
                             if (!ok) break;
                             tc_fence_after();
@@ -367,9 +381,9 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
             }
             for (int t = 0; t < C::TILES && ok; ++t) {   // tiles whose last block is the CTA's last
                 if (nkv_t(t) == 0 || jhi(t) != jbeg + nkv) continue;
-                ok = mbar_wait(&bar_p[t], (jhi(t) - 1 - jlo(t)) & 1, s_abort);
+                ok = mbar_wait(&bar_p[t], (jhi(t) - 1 - jlo(t)) & 1, s_abort, lim);
                 if (ok && !v_ready) {
-                    ok = mbar_wait(&full[v_slot], v_phase, s_abort);
+                    ok = mbar_wait(&full[v_slot], v_phase, s_abort, lim);
                     v_ready = true;
                 }
                 if (!ok) break;
@@ -380,7 +394,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
             // Drain: no MMA of this CTA is in flight at teardown.
             tc_commit(bar_fin);
             volatile int no_abort = 0;
-            mbar_wait(bar_fin, 0, &no_abort);
+            mbar_wait(bar_fin, 0, &no_abort, lim);
         }
         __syncwarp();
     } else {
@@ -398,7 +412,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
         float l = 0.f;
         bool ok = true;
         for (int j = jlo(t); j < jhi(t); ++j) {
-            if (!mbar_wait_warp(&bar_s[t], (j - jlo(t)) & 1, s_abort)) {
+            if (!mbar_wait_warp(&bar_s[t], (j - jlo(t)) & 1, s_abort, lim)) {
                 ok = false;
                 break;
             }
@@ -587,7 +601,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
         }
         // ---- epilogue: O = acc / l (times 1/(1-p)), LSE = (m + log2 l) ln 2 ----
         if (ok && ntile > 0) {
-            ok = mbar_wait_warp(&bar_o[t], 0, s_abort);
+            ok = mbar_wait_warp(&bar_o[t], 0, s_abort, lim);
             tc_fence_after();
         }
         if (ok) {
@@ -653,11 +667,12 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8>::THREADS,
 }
 
 template <int D, bool kTF32, bool kF16, bool kFP8, bool kCausal, bool kDropout, bool kWindow,
-          bool kPacked>
+          bool kPacked, int kTiles, bool kSelfTest = false>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const FwdParams& p, cudaStream_t stream) {
-    using C = FwdCfg<D, kTF32, kF16, kFP8>;
-    auto kern = attn_fwd_kernel<D, kTF32, kF16, kFP8, kCausal, kDropout, kWindow, kPacked>;
+    using C = FwdCfg<D, kTF32, kF16, kFP8, kTiles>;
+    auto kern = attn_fwd_kernel<D, kTF32, kF16, kFP8, kCausal, kDropout, kWindow, kPacked, kTiles,
+                                kSelfTest>;
     static std::atomic<unsigned long long> smem_ready{0};
     const cudaError_t e = enable_smem_per_device(kern, C::SMEM, smem_ready);
     if (e != cudaSuccess) return e;
@@ -668,21 +683,22 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     return cudaGetLastError();
 }
 
-template <int D, bool kTF32, bool kF16, bool kFP8, bool kPacked, bool kWindow>
+template <int D, bool kTF32, bool kF16, bool kFP8, bool kPacked, bool kWindow, int kTiles>
 cudaError_t dispatch_mask_w(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, bool causal, bool dropout, cudaStream_t s) {
     if (causal)
-        return dropout ? launch_fwd_t<D, kTF32, kF16, kFP8, true, true, kWindow, kPacked>(tq, tk, tv, p, s)
-                       : launch_fwd_t<D, kTF32, kF16, kFP8, true, false, kWindow, kPacked>(tq, tk, tv, p, s);
-    return dropout ? launch_fwd_t<D, kTF32, kF16, kFP8, false, true, kWindow, kPacked>(tq, tk, tv, p, s)
-                   : launch_fwd_t<D, kTF32, kF16, kFP8, false, false, kWindow, kPacked>(tq, tk, tv, p, s);
+        return dropout ? launch_fwd_t<D, kTF32, kF16, kFP8, true, true, kWindow, kPacked, kTiles>(tq, tk, tv, p, s)
+                       : launch_fwd_t<D, kTF32, kF16, kFP8, true, false, kWindow, kPacked, kTiles>(tq, tk, tv, p, s);
+    return dropout ? launch_fwd_t<D, kTF32, kF16, kFP8, false, true, kWindow, kPacked, kTiles>(tq, tk, tv, p, s)
+                   : launch_fwd_t<D, kTF32, kF16, kFP8, false, false, kWindow, kPacked, kTiles>(tq, tk, tv, p, s);
 }
 
-template <int D, bool kTF32, bool kF16, bool kFP8, bool kPacked>
+// kTiles query tiles per CTA; head dim 256 always takes one.
+template <int D, bool kTF32, bool kF16, bool kFP8, bool kPacked, int kTiles = (D == 256 ? 1 : 2)>
 cudaError_t dispatch_mask(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const FwdParams& p, bool causal, bool dropout, cudaStream_t s) {
-    return p.window > 0 ? dispatch_mask_w<D, kTF32, kF16, kFP8, kPacked, true>(tq, tk, tv, p, causal, dropout, s)
-                        : dispatch_mask_w<D, kTF32, kF16, kFP8, kPacked, false>(tq, tk, tv, p, causal, dropout, s);
+    return p.window > 0 ? dispatch_mask_w<D, kTF32, kF16, kFP8, kPacked, true, kTiles>(tq, tk, tv, p, causal, dropout, s)
+                        : dispatch_mask_w<D, kTF32, kF16, kFP8, kPacked, false, kTiles>(tq, tk, tv, p, causal, dropout, s);
 }
 
 }  // namespace

@@ -6,7 +6,9 @@ namespace gbattn {
 
 cudaError_t launch_fwd_packed(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const FwdParams& p, int d, attn_dtype dtype, bool causal,
-                              bool dropout, cudaStream_t stream) {
+                              bool dropout, int tiles, cudaStream_t stream) {
+    if (tiles == 1 && d <= 128 && (dtype == ATTN_DTYPE_BF16 || dtype == ATTN_DTYPE_FP16))
+        return launch_fwd_packed_1tile(tq, tk, tv, p, d, dtype, causal, dropout, stream);
     switch (dtype) {
         case ATTN_DTYPE_BF16:
             if (d == 64) return dispatch_mask<64, false, false, false, true>(tq, tk, tv, p, causal, dropout, stream);

@@ -11,9 +11,8 @@
 
 namespace gbattn {
 
-// Rows per query / key tile (the MMA's M) and query tiles per forward CTA.
+// Rows per query / key tile (the MMA's M).
 constexpr int kTileRows = 128;
-constexpr int kFwdTilesPerCta = 2;
 
 // Where the rows of a sequence live.  Dense (cu == nullptr): activations
 // [B, H, N, d] and per-row values (LSE) [B, H, N].  Packed sequences
@@ -42,6 +41,11 @@ struct FwdParams {
     uint32_t seed_lo, seed_hi;
     int window;               // > 0: sliding window of this many keys
     SeqLayout lq, lk;         // query / key row placement (N, Nk are their N)
+    // Read only by the self-test instantiation of the forward (see
+    // attn_selftest_fwd_withheld): the key block whose K tile the producer
+    // withholds, and the wait limit that replaces the default.
+    int withhold_block;
+    unsigned long long wait_ns;
 };
 
 struct BwdParams {
@@ -96,15 +100,32 @@ attn_status check_bwd_args(const void* Q, const void* K, const void* V, const vo
                            const void* dV, int B, int H, int N, int Nk, int d, attn_dtype dtype,
                            float scale, float dropout_p);
 
-// Forward launch (validated arguments only).
+// Query tiles of 128 rows per forward CTA: 2 (the tiles share every K/V
+// block; one CTA per SM) or 1 (two CTAs per SM).  Head dim 256, fp32 and e4m3
+// inputs always take their one layout (1, 2 and 2 tiles).  For bf16 and fp16
+// with d <= 128 the environment variable GBATTN_FWD_TILES ("1" or "2", read
+// at each call) decides; without it, 1 for d = 64 with N <= 2048 query rows
+// (the longest sequence when packed), else 2.
+int fwd_tiles(int d, attn_dtype dtype, int N);
+
+// Forward launch (validated arguments only) with `tiles` query tiles per CTA.
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int d, attn_dtype dtype, bool causal, bool dropout,
-                       cudaStream_t stream);
+                       int tiles, cudaStream_t stream);
 
-// The same for packed sequences (p.lq.cu != nullptr; bf16 or fp16).
+// The same for packed sequences (p.lq.cu != nullptr; bf16, fp16 or e4m3).
 cudaError_t launch_fwd_packed(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const FwdParams& p, int d, attn_dtype dtype, bool causal,
-                              bool dropout, cudaStream_t stream);
+                              bool dropout, int tiles, cudaStream_t stream);
+
+// One query tile per CTA, bf16 or fp16 with d in {64, 128}: dense and packed.
+cudaError_t launch_fwd_1tile(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const FwdParams& p, int d, attn_dtype dtype, bool causal, bool dropout,
+                             cudaStream_t stream);
+cudaError_t launch_fwd_packed_1tile(const CUtensorMap& tq, const CUtensorMap& tk,
+                                    const CUtensorMap& tv, const FwdParams& p, int d,
+                                    attn_dtype dtype, bool causal, bool dropout,
+                                    cudaStream_t stream);
 
 // Backward launches (validated arguments only).
 // f16: the 16-bit tensors are IEEE half (else bf16).

@@ -60,14 +60,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Single-thread bounded wait for the phase of `bar` with the given parity.
 // Returns false (and raises *abort) when the limit expires or another role has
 // already raised *abort.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31u) == 0) {
             if (*abort) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 *abort = 1;
                 return false;
             }
@@ -79,13 +80,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // same answer, so the warp stays converged for the .sync.aligned tcgen05
 // instructions that follow.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
-                                               volatile int* abort) {
+                                               volatile int* abort,
+                                               unsigned long long limit_ns = kWaitLimitNs) {
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 0;; ++it) {
         const bool ok = mbar_try_wait(bar, parity);
         if (__all_sync(0xffffffffu, ok)) return true;
         if ((it & 31u) == 31u) {
-            int give_up = (*abort != 0) || (globaltimer() - t0 > kWaitLimitNs);
+            int give_up = (*abort != 0) || (globaltimer() - t0 > limit_ns);
             give_up = __shfl_sync(0xffffffffu, give_up, 0);
             if (give_up) {
                 *abort = 1;

@@ -73,6 +73,12 @@
  *             out-of-range key length) are written to *dev_status (a device
  *             int, 0 = OK) when dev_status is not NULL; the kernel then exits
  *             cleanly and leaves the affected outputs unspecified.
+ *  Tuning     The forward runs two 128-row query tiles per CTA (one CTA per
+ *             SM) or, for bf16 and fp16 with d <= 128, one tile per CTA (two
+ *             CTAs per SM): one tile by default for d = 64 with N <= 2048,
+ *             else two; the environment variable GBATTN_FWD_TILES ("1" or
+ *             "2", read at each call) overrides the choice.  The result does
+ *             not depend on it.
  *  Threads    Every entry point is thread-safe.
  *  Devices    One process may drive several GPUs: every call runs on the
  *             device current in the calling thread (cudaSetDevice), whose
@@ -243,6 +249,25 @@ attn_status attn_bwd_varlen(const void* Q, const void* K, const void* V, const v
  * expiry leaves the context usable.  Not part of the attention path.
  */
 attn_status attn_selftest_wait(int* dev_status, int arrive, void* stream);
+
+/*
+ * Device self-test of the fused forward kernel's own abort path.  It runs the
+ * bf16, d = 128, non-causal forward (the kernel of attn_fwd, in a test
+ * instantiation that only this entry point launches) on Q [B, H, N, 128] and
+ * K, V [B, H, Nk, 128], with two changes: the producer never issues the copy
+ * of the K tile of key block withhold_block (a tile withheld, not a fault:
+ * nothing ever completes that tile's barrier), and every wait gives up after
+ * wait_ms milliseconds (1 to 2000) instead of about 2 s.  A CTA that walks
+ * that key block then has copies and MMAs in flight when its wait expires: it
+ * drains them, frees its tensor memory, writes ATTN_ERR_DEVICE_TIMEOUT to
+ * *dev_status (required, a device int, 0 on entry) and returns; O and LSE of
+ * such CTAs are unspecified.  withhold_block < 0 withholds nothing and gives
+ * the ordinary result.  Not part of the attention path.
+ */
+attn_status attn_selftest_fwd_withheld(const void* Q, const void* K, const void* V, void* O,
+                                       float* LSE, int B, int H, int N, int Nk,
+                                       int withhold_block, int wait_ms, int* dev_status,
+                                       void* stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char* attn_status_string(attn_status status);

@@ -150,6 +150,9 @@ def attn_fwd(Q, K, V, scale=None, causal=False, key_lens=None, dropout_p=0.0, se
     L = _lib or lib()
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     B, H, N, d = Q.shape
+    if K.shape != Q.shape or V.shape != Q.shape:
+        raise ValueError("attn_fwd takes square problems (K, V shaped like Q); "
+                         "use attn_fwd_bwd_qk for N_k != N")
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     kl = _key_lens(key_lens, B, N)
@@ -174,6 +177,9 @@ def attn_bwd(Q, K, V, dO, scale=None, causal=False, key_lens=None, dropout_p=0.0
     L = _lib or lib()
     Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
     B, H, N, d = Q.shape
+    if K.shape != Q.shape or V.shape != Q.shape or dO.shape != Q.shape:
+        raise ValueError("attn_bwd takes square problems (K, V, dO shaped like Q); "
+                         "use attn_fwd_bwd_qk for N_k != N")
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     kl = _key_lens(key_lens, B, N)

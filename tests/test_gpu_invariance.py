@@ -1,4 +1,5 @@
-"""Key-shift invariance of exact attention, checked on the GPU's own outputs.
+"""Invariances of exact attention checked on the GPU's own outputs: key shift
+and tile size.
 
 Adding one vector c to every key adds scale * (q_i . c) to every score of
 row i, so each softmax row is unchanged ("Why FlashAttention Is a Kernel
@@ -16,7 +17,8 @@ import pytest
 import torch
 
 import exact_attention_58_gb300 as ea
-from exact_attention_58_gb300.workloads import make_inputs
+import oracle
+from exact_attention_58_gb300.workloads import make_inputs, make_packed_inputs
 from gpu_helpers import GRAD_RTOL, LSE_ATOL, O_ATOL, f64, grad_err, lse_err, oracle_bwd, oracle_fwd
 
 pytestmark = pytest.mark.gpu
@@ -76,3 +78,78 @@ def test_key_shift_leaves_o_and_gradients_and_moves_lse(d, causal, pad, p):
     assert lse_err(f64(l2), L_ref + shift.numpy()) <= LSE_ATOL
     for a, b_ in ((dq1, dq2), (dk1, dk2), (dv1, dv2)):
         assert grad_err(f64(b_), f64(a)) <= GRAD_RTOL
+
+
+# ---------------------------------------------------------------------------
+# Tile-size invariance on the GPU: the forward run with one and with two
+# 128-row query tiles per CTA (GBATTN_FWD_TILES, read at each call).  The
+# pages' tiled result is the full softmax whatever the tiling ("Tiling:
+# fitting the work inside SRAM"): each layout must meet the tolerance against
+# the oracle, and the two must agree to 1e-2.
+# ---------------------------------------------------------------------------
+def _with_tiles(monkeypatch, tiles, fn):
+    monkeypatch.setenv("GBATTN_FWD_TILES", str(tiles))
+    try:
+        return fn()
+    finally:
+        monkeypatch.delenv("GBATTN_FWD_TILES")
+
+
+@pytest.mark.parametrize("d,causal,pad,p,window", [
+    (64, True, False, 0.0, 0),
+    (128, True, False, 0.0, 0),
+    (64, False, True, 0.1, 0),
+    (128, False, True, 0.0, 0),
+    (128, True, False, 0.0, 200),
+    (64, False, False, 0.1, 150),
+])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_one_and_two_query_tiles_per_cta_agree(monkeypatch, d, causal, pad, p, window, dtype):
+    B, H, N = 2, 3, 645   # 5 tiles of 128 rows and a ragged 5-row tail: odd tile counts
+    inp = make_inputs(B, H, N, d, dtype=dtype, gen_seed=900 + d + 5 * causal + 3 * pad,
+                      causal=causal, key_len_range=(300, N) if pad else None, dropout_p=p,
+                      dropout_seed_value=0x5EED9000 + d, with_do=False)
+    inp.window = window
+    q, k, v = (t.cuda() for t in (inp.q, inp.k, inp.v))
+    kl = None if inp.key_lens is None else inp.key_lens.cuda()
+
+    def run():
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        o, lse = ea.attn_fwd(q, k, v, causal=causal, key_lens=kl, dropout_p=p, seed=inp.seed,
+                             scale=inp.scale, window=window, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        return o, lse
+
+    o1, l1 = _with_tiles(monkeypatch, 1, run)
+    o2, l2 = _with_tiles(monkeypatch, 2, run)
+    O_ref, L_ref = oracle_fwd(inp)
+    for o, lse in ((o1, l1), (o2, l2)):
+        assert np.abs(f64(o) - O_ref).max() <= O_ATOL
+        assert lse_err(f64(lse), L_ref) <= LSE_ATOL
+    assert float((o1.float() - o2.float()).abs().max()) <= 1e-2
+    assert lse_err(f64(l1), f64(l2)) <= 1e-2
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_one_and_two_query_tiles_per_cta_agree_packed(monkeypatch, d):
+    lens = [1, 300, 77, 129, 256, 0, 513]
+    inp = make_packed_inputs(lens, lens, 2, d, gen_seed=950 + d, causal=True)
+    q, k, v = (t.cuda() for t in (inp.q, inp.k, inp.v))
+    cu = inp.cu_q.cuda()
+
+    def run():
+        o, lse = ea.attn_fwd_varlen(q, k, v, cu, cu, inp.max_q, inp.max_k, causal=True,
+                                    scale=inp.scale)
+        torch.cuda.synchronize()
+        return o, lse
+
+    o1, l1 = _with_tiles(monkeypatch, 1, run)
+    o2, l2 = _with_tiles(monkeypatch, 2, run)
+    O_ref, L_ref, *_ = oracle.attn_fwd_bwd_varlen(f64(inp.q), f64(inp.k), f64(inp.v),
+                                                  f64(inp.do), inp.cu_q.numpy(), inp.cu_k.numpy(),
+                                                  inp.scale, True, 0.0, 0)
+    for o, lse in ((o1, l1), (o2, l2)):
+        assert np.abs(f64(o) - O_ref).max() <= O_ATOL
+        assert lse_err(f64(lse), L_ref) <= LSE_ATOL
+    assert float((o1.float() - o2.float()).abs().max()) <= 1e-2

@@ -33,3 +33,34 @@ def test_expired_wait_reports_timeout_and_the_context_survives():
     o, _ = gpu_fwd(inp)
     O_ref, _ = oracle_fwd(inp)
     assert float(np.abs(f64(o) - O_ref).max()) <= O_ATOL
+
+
+def test_withheld_tile_makes_the_forward_abort_cleanly():
+    """The fused forward itself (test instantiation): with one K tile never
+    loaded, the MMA warp's wait for it expires after 20 ms while other copies
+    and products are in flight; every CTA drains, frees its tensor memory and
+    reports ATTN_ERR_DEVICE_TIMEOUT, the call returns, and the context keeps
+    working (a normal forward afterwards matches the oracle)."""
+    B, H, N = 1, 2, 640   # six CTAs, each walking five key blocks
+    inp = make_inputs(B, H, N, 128, gen_seed=31, with_do=False)
+    q, k, v = (t.cuda() for t in (inp.q, inp.k, inp.v))
+    O_ref, L_ref = oracle_fwd(inp)
+    # control: nothing withheld, the ordinary result
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, lse = ea.attn_selftest_fwd_withheld(q, k, v, st, withhold_block=-1, wait_ms=20)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert float(np.abs(f64(o) - O_ref).max()) <= O_ATOL
+    # the K tile of key block 0, 2 or 4 withheld
+    for block in (0, 2, 4):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        t0 = time.monotonic()
+        ea.attn_selftest_fwd_withheld(q, k, v, st, withhold_block=block, wait_ms=20)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 6, (block, int(st.item()))   # ATTN_ERR_DEVICE_TIMEOUT
+        assert time.monotonic() - t0 < 10.0
+    # the context is intact: the product path still gives the oracle's result
+    inp2 = make_inputs(2, 3, 300, 128, gen_seed=32, causal=True)
+    o2, _ = gpu_fwd(inp2)
+    O2_ref, _ = oracle_fwd(inp2)
+    assert float(np.abs(f64(o2) - O2_ref).max()) <= O_ATOL
