@@ -38,8 +38,8 @@ attn_status check_shape(int B, int H, int N, int d, attn_dtype dtype, bool backw
         dtype != ATTN_DTYPE_FP8_E4M3)
         return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
-    if (d == 256 && (backward || (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP16)))
-        return ATTN_ERR_UNSUPPORTED;   // head dim 256: 16-bit forward only
+    if (d == 256 && dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP16)
+        return ATTN_ERR_UNSUPPORTED;   // head dim 256: 16-bit types
     if (dtype == ATTN_DTYPE_FP32 && (backward || d != 64)) return ATTN_ERR_UNSUPPORTED;
     if (dtype == ATTN_DTYPE_FP8_E4M3 && (backward || d != 128)) return ATTN_ERR_UNSUPPORTED;
     const long long elems = static_cast<long long>(B) * H * npad_of(N) * d;
@@ -129,33 +129,36 @@ int fwd_tiles(int d, attn_dtype dtype, int N) {
     return (d == 64 && N <= 2048) ? 1 : 2;
 }
 
-bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int BH, int N, int d) {
+bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int BH, int N, int d,
+                    int rows) {
     const cuuint64_t es = elem_bytes(dtype);
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es,
                                    static_cast<cuuint64_t>(N) * d * es};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(kTileRows), 1};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(rows), 1};
     return encode_3d(map, ptr, dtype, dims, strides, box);
 }
 
-bool make_tmap_thd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int T, int H, int d) {
+bool make_tmap_thd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int T, int H, int d,
+                   int rows) {
     const cuuint64_t es = elem_bytes(dtype);
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                                 static_cast<cuuint64_t>(T)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es,
                                    static_cast<cuuint64_t>(H) * d * es};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 1, static_cast<cuuint32_t>(kTileRows)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 1, static_cast<cuuint32_t>(rows)};
     return encode_3d(map, ptr, dtype, dims, strides, box);
 }
 
 namespace {
 
-// Map over one activation tensor: [B*H][N][d] when dense, [T][H][d] when packed.
+// Map over one activation tensor: [B*H][N][d] when dense, [T][H][d] when
+// packed; boxes of `rows` rows.
 bool make_tmap(CUtensorMap* map, const void* ptr, attn_dtype dtype, int B, const SeqLayout& l,
-               int d) {
-    return l.cu ? make_tmap_thd(map, ptr, dtype, l.total, l.H, d)
-                : make_tmap_bhnd(map, ptr, dtype, B * l.H, l.N, d);
+               int d, int rows = kTileRows) {
+    return l.cu ? make_tmap_thd(map, ptr, dtype, l.total, l.H, d, rows)
+                : make_tmap_bhnd(map, ptr, dtype, B * l.H, l.N, d, rows);
 }
 
 // Checks of the packed-sequence entry points, on top of those of the dense
@@ -231,9 +234,11 @@ attn_status main_impl(const void* Q, const void* K, const void* V, const void* d
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(dK) ||
         !aligned16(dV))
         return ATTN_ERR_MISALIGNED;
+    // head dim 256 walks 64-row query blocks: Q and dO boxes of 64 rows
+    const int qrows = d == 256 ? 64 : kTileRows;
     CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-    if (!make_tmap(&tq, Q, dtype, B, lq, d) || !make_tmap(&tk, K, dtype, B, lk, d) ||
-        !make_tmap(&tv, V, dtype, B, lk, d) || !make_tmap(&tdo, dO, dtype, B, lq, d) ||
+    if (!make_tmap(&tq, Q, dtype, B, lq, d, qrows) || !make_tmap(&tk, K, dtype, B, lk, d) ||
+        !make_tmap(&tv, V, dtype, B, lk, d) || !make_tmap(&tdo, dO, dtype, B, lq, d, qrows) ||
         !make_tmap(&tdk, dK, dtype, B, lk, d) || !make_tmap(&tdv, dV, dtype, B, lk, d))
         return ATTN_ERR_CUDA;
     const Workspace w = carve(workspace, B, lq.H, lq.N);
@@ -260,6 +265,10 @@ attn_status main_impl(const void* Q, const void* K, const void* V, const void* d
     p.window = window > 0 ? window : 0;
     p.lq = lq;
     p.lk = lk;
+    if (d == 256)
+        return from_cuda(launch_bwd_main_d256(tq, tk, tv, tdo, tdk, tdv, p,
+                                              dtype == ATTN_DTYPE_FP16, causal != 0,
+                                              dropout_p > 0.f, static_cast<cudaStream_t>(stream)));
     return from_cuda(launch_bwd_main(tq, tk, tv, tdo, tdk, tdv, p, d, dtype == ATTN_DTYPE_FP16,
                                      causal != 0, dropout_p > 0.f,
                                      static_cast<cudaStream_t>(stream)));

@@ -144,6 +144,9 @@ cudaError_t launch_bwd_pre(const void* O, const void* dO, const float* LSE, floa
     } else if (d == 128) {
         if (f16) launch_pre_t<128, true>(grid, O, dO, LSE, lse2, Drow, dq_acc, BH, lq, Npad, stream);
         else launch_pre_t<128, false>(grid, O, dO, LSE, lse2, Drow, dq_acc, BH, lq, Npad, stream);
+    } else if (d == 256) {
+        if (f16) launch_pre_t<256, true>(grid, O, dO, LSE, lse2, Drow, dq_acc, BH, lq, Npad, stream);
+        else launch_pre_t<256, false>(grid, O, dO, LSE, lse2, Drow, dq_acc, BH, lq, Npad, stream);
     } else {
         return cudaErrorInvalidValue;
     }

@@ -85,12 +85,15 @@ cudaError_t enable_smem_per_device(Kernel kern, int bytes, std::atomic<unsigned 
     return e;
 }
 
-// Tensor map over a contiguous [B*H][N][d] array, 128-row boxes of 128 bytes
-// along d, 128-byte swizzle.  Returns false if the driver rejected it.
-bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int BH, int N, int d);
+// Tensor map over a contiguous [B*H][N][d] array, boxes of `rows` rows (128
+// unless given) and 128 bytes along d, 128-byte swizzle.  Returns false if the
+// driver rejected it.
+bool make_tmap_bhnd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int BH, int N, int d,
+                    int rows = kTileRows);
 // Tensor map over a contiguous [T][H][d] array (packed sequences) with the
-// same boxes: 128 consecutive tokens of one head, 128 bytes along d.
-bool make_tmap_thd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int T, int H, int d);
+// same boxes: `rows` consecutive tokens of one head, 128 bytes along d.
+bool make_tmap_thd(CUtensorMap* map, const void* ptr, attn_dtype dtype, int T, int H, int d,
+                   int rows = kTileRows);
 
 // Every check attn_bwd makes before it looks at the workspace: NULL pointers,
 // shape, key count, scale, dropout probability and 16-byte alignment, in that
@@ -145,6 +148,13 @@ cudaError_t launch_bwd_main_packed(const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tdk, const CUtensorMap& tdv,
                                    const BwdParams& p, int d, bool f16, bool causal, bool dropout,
                                    cudaStream_t stream);
+// The main launch at head dim 256 (dense or packed by p.lq.cu): Q and dO maps
+// with 64-row boxes, the others with 128-row boxes.
+cudaError_t launch_bwd_main_d256(const CUtensorMap& tq64, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const CUtensorMap& tdo64,
+                                 const CUtensorMap& tdk, const CUtensorMap& tdv,
+                                 const BwdParams& p, bool f16, bool causal, bool dropout,
+                                 cudaStream_t stream);
 cudaError_t launch_bwd_dq_convert(void* dQ, const float* dq_acc, int BH, const SeqLayout& lq,
                                   int Npad, int d, bool f16, float scale, cudaStream_t stream);
 

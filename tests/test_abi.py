@@ -106,7 +106,8 @@ def _bwd(lib, **kw):
     (dict(dtype=2, d=96), 2),
     (dict(dtype=3), 2),            # e4m3: forward only
     (dict(dtype=3, d=128), 2),
-    (dict(d=256), 2),              # head dim 256: forward only
+    (dict(d=256, dtype=1), 2),     # head dim 256: 16-bit types only
+    (dict(d=512), 2),
     (dict(dtype=4), 1),
     (dict(d=80), 2),
     (dict(ws=None), 4),
