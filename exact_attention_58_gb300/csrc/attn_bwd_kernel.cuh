@@ -40,10 +40,13 @@ namespace {
 //   warp  12   TMA producer: K_j, V_j once; Q_i, dO_i, LSE_i, D_i per block
 //   warp  13   MMA issuer.  S^T and dP^T are committed separately: the
 //              compute warps build P from S^T while dP^T runs, dV for each
-//              query half starts as soon as its P is in TMEM, and dK for each
-//              half as soon as its dS is in shared memory.  Across blocks the
-//              issue order is  dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1}, so the
-//              next S^T is computed while the compute warps build dS_i.
+//              query half starts as soon as its P is in TMEM, and dQ and dK
+//              for each half as soon as its dS is in shared memory.  Across
+//              blocks the issue order is  dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1}
+//              at d = 64 and  dV_i, dQ_i and dK_i of query half 0, S_{i+1},
+//              dQ_i and dK_i of half 1, dP_{i+1}  at d = 128, where the dQ
+//              warps' fp32 adds (64 KB a block) set the pace: their first
+//              half is handed over as early as possible.
 //
 // Tensor memory (512 columns):
 //   d = 64:  dK [0,64) dV [64,128) S [128,256) dP [256,384) dQ [384,448)
@@ -302,11 +305,10 @@ __global__ void __launch_bounds__(448, 1)
                 return true;
             };
             // Software pipeline over query blocks: S^T of block i+1 is issued
-            // right behind dV of block i (the tensor pipe runs one thread's MMAs
-            // in issue order, so it reads P_i before S^T_{i+1} overwrites it),
-            // and dP^T of block i+1 right behind dQ and dK of block i.  The
-            // compute warps then always find the next S^T on its way while
-            // they build dS.
+            // behind dV of block i (the tensor pipe runs one thread's MMAs in
+            // issue order, so it reads P_i before S^T_{i+1} overwrites it), and
+            // dP^T of block i+1 right behind dQ and dK of block i.  The compute
+            // warps then find the next S^T on its way while they build dS.
             bool ok = mbar_wait(bar_kv, 0, s_abort) && mbar_wait(&full_q[0], 0, s_abort);
             if (ok) {
                 tc_fence_after();
@@ -328,12 +330,19 @@ __global__ void __launch_bounds__(448, 1)
                     issue_dv_half(hh, do_mn, it == 0 && hh == 0);
                 }
                 if (!ok) break;
-                if (more) {
+                auto issue_next_s = [&]() {
                     ok = mbar_wait(&full_q[nstage], ((it + 1) >> 1) & 1, s_abort);
-                    if (!ok) break;
+                    if (!ok) return;
                     tc_fence_after();
                     issue_s(nstage);
                     tc_commit(bar_S);
+                };
+                // d = 64: the next S^T right behind dV (the compute warps need it
+                // soonest); d = 128: after dQ and dK of the first query half, so
+                // that dQ^T half 0 (which the dQ warps then drain) goes first
+                if (D == 64 && more) {
+                    issue_next_s();
+                    if (!ok) break;
                 }
                 // d = 128: dQ^T = K^T dS^T for one query half needs only that
                 // half of dS, so it follows dK of the half straight away.
@@ -348,8 +357,12 @@ __global__ void __launch_bounds__(448, 1)
                 ok = mbar_wait(&bar_dS[0], it & 1, s_abort);
                 if (!ok) break;
                 tc_fence_after();
-                issue_dk_half(0, q_mn, it == 0);
                 if constexpr (D == 128) issue_dq_half(0);
+                issue_dk_half(0, q_mn, it == 0);
+                if (D == 128 && more) {
+                    issue_next_s();
+                    if (!ok) break;
+                }
                 ok = mbar_wait(&bar_dS[1], it & 1, s_abort);
                 if (ok && D == 64 && it > 0) ok = mbar_wait(&bar_dQfree[0], (it - 1) & 1, s_abort);
                 if (!ok) break;
