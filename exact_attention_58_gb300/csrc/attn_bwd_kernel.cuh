@@ -256,39 +256,40 @@ __global__ void __launch_bounds__(448, 1)
             const uint64_t dO_mn0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), C::CB_BYTES, 1024);
             // dV += P^T dO (P from TMEM) and dK += dS^T Q (dS from smem) over the
             // query columns [64 hh, 64 hh + 64)
+            // Each group of MMAs is issued as one run (ptx.cuh): the MMA warp
+            // shares its sub-partition with busy compute warps, so its own
+            // instruction count sets how fast the products reach the queue.
+            constexpr uint32_t CB = C::CB_BYTES / 16 - 6;   // K-major: next column block after 4 steps
             auto issue_dv_half = [&](int hh, uint64_t do_mn, bool first) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ts<false>(tmem + C::C_DV, tmem + C::C_S + 64 * hh + 8 * kk,
-                                  sdesc_adv(do_mn, (4 * hh + kk) * 2048), C::IDESC_DKV,
-                                  (first && kk == 0) ? 0u : 1u);
+                // dV += P^T dO: 4 x 16 queries, P from TMEM, dO MN-major
+                mma_run_ts_f16<4, 8, 128>(tmem + C::C_DV, tmem + C::C_S + 64 * hh,
+                                          sdesc_adv(do_mn, 4 * hh * 2048), C::IDESC_DKV,
+                                          first ? 0u : 1u);
             };
             auto issue_dk_half = [&](int hh, uint64_t q_mn, bool first) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ss<false>(tmem + C::C_DK, sdesc_adv(dS_k, hh * C::CB_BYTES + 32 * kk),
-                                  sdesc_adv(q_mn, (4 * hh + kk) * 2048), C::IDESC_DKV,
-                                  (first && kk == 0) ? 0u : 1u);
+                // dK += dS^T Q: A = dS read with keys as rows (32-byte steps), Q MN-major
+                mma4_ss_f16<2, 2, 2, 128, 128, 128>(tmem + C::C_DK, sdesc_adv(dS_k, hh * C::CB_BYTES),
+                                                    sdesc_adv(q_mn, 4 * hh * 2048), C::IDESC_DKV,
+                                                    first ? 0u : 1u);
             };
             auto issue_s = [&](int stage) {   // S^T = K Q^T
                 const uint64_t q_k = sdesc_adv(dQ_k0, stage * C::TILE);
-#pragma unroll
-                for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::CB_BYTES + (kk & 3) * 32;
-                    mma_ss<false>(tmem + C::C_S, sdesc_adv(dK_k, off), sdesc_adv(q_k, off),
-                                  C::IDESC_SDP, kk > 0);
-                }
+                if constexpr (C::QK_STEPS == 8)
+                    mma8_ss_f16<2, 2, 2, CB, 2, 2, 2, 2, 2, 2, CB, 2, 2, 2>(tmem + C::C_S, dK_k, q_k,
+                                                                          C::IDESC_SDP, 0u);
+                else
+                    mma4_ss_f16<2, 2, 2, 2, 2, 2>(tmem + C::C_S, dK_k, q_k, C::IDESC_SDP, 0u);
             };
             // dP^T = V dO^T for the query columns [64 hh, 64 hh + 64) (N = 64:
             // B is rows 64 hh.. of the dO tile)
             auto issue_dp_half = [&](int stage, int hh) {
                 const uint64_t do_k = sdesc_adv(dO_k0, stage * C::TILE + hh * C::HALF_BYTES);
-#pragma unroll
-                for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::CB_BYTES + (kk & 3) * 32;
-                    mma_ss<false>(tmem + C::C_DP + 64 * hh, sdesc_adv(dV_k, off),
-                                  sdesc_adv(do_k, off), C::IDESC_DP_HALF, kk > 0);
-                }
+                if constexpr (C::QK_STEPS == 8)
+                    mma8_ss_f16<2, 2, 2, CB, 2, 2, 2, 2, 2, 2, CB, 2, 2, 2>(
+                        tmem + C::C_DP + 64 * hh, dV_k, do_k, C::IDESC_DP_HALF, 0u);
+                else
+                    mma4_ss_f16<2, 2, 2, 2, 2, 2>(tmem + C::C_DP + 64 * hh, dV_k, do_k,
+                                                  C::IDESC_DP_HALF, 0u);
             };
             // d = 128: the next dP^T half may only land once the dQ warps have
             // read the dQ^T half that shares its columns.
@@ -346,12 +347,9 @@ __global__ void __launch_bounds__(448, 1)
                 }
                 // d = 128: dQ^T = K^T dS^T for one query half needs only that
                 // half of dS, so it follows dK of the half straight away.
-                auto issue_dq_half = [&](int hh) {
-#pragma unroll
-                    for (int kk = 0; kk < kTileRows / 16; ++kk)   // K = keys
-                        mma_ss<false>(tmem + C::C_DQ + 64 * hh, sdesc_adv(dK_mn, kk * 2048),
-                                      sdesc_adv(dS_mn, hh * C::CB_BYTES + kk * 2048),
-                                      C::IDESC_DQ, kk > 0);
+                auto issue_dq_half = [&](int hh) {   // K = keys, 8 x 16 rows
+                    mma8_ss_f16<128, 128, 128, 128, 128, 128, 128, 128, 128, 128, 128, 128, 128, 128>(
+                        tmem + C::C_DQ + 64 * hh, dK_mn, sdesc_adv(dS_mn, hh * C::CB_BYTES), C::IDESC_DQ, 0u);
                     tc_commit(&bar_dQ[hh]);
                 };
                 ok = mbar_wait(&bar_dS[0], it & 1, s_abort);
@@ -367,11 +365,9 @@ __global__ void __launch_bounds__(448, 1)
                 if (ok && D == 64 && it > 0) ok = mbar_wait(&bar_dQfree[0], (it - 1) & 1, s_abort);
                 if (!ok) break;
                 tc_fence_after();
-                if constexpr (D == 64) {   // dQ = dS K (lanes = queries)
-#pragma unroll
-                    for (int kk = 0; kk < kTileRows / 16; ++kk)   // K = keys
-                        mma_ss<false>(tmem + C::C_DQ, sdesc_adv(dS_mn, kk * 2048),
-                                      sdesc_adv(dK_mn, kk * 2048), C::IDESC_DQ, kk > 0);
+                if constexpr (D == 64) {   // dQ = dS K (lanes = queries), K = keys
+                    mma8_ss_f16<128, 128, 128, 128, 128, 128, 128, 128, 128, 128, 128, 128, 128, 128>(
+                        tmem + C::C_DQ, dS_mn, dK_mn, C::IDESC_DQ, 0u);
                     tc_commit(&bar_dQ[0]);
                 } else {
                     issue_dq_half(1);

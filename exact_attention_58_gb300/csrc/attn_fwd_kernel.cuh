@@ -302,6 +302,22 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8, kTiles>::THREADS,
                 const uint32_t d_tmem = tmem + 128u * t;
                 const uint64_t ad = t ? dq1 : dq0;
                 const uint64_t bd = sdesc_adv(dk0, slot * C::TILE);
+                // 16-bit inputs: one run of MMAs (32-byte K steps, the next
+                // 128-byte column block after four)
+                constexpr uint32_t CB = C::CB_BYTES / 16 - 6;
+                if constexpr (!kTF32 && !kFP8 && C::QK_STEPS == 8) {
+                    mma8_ss_f16<2, 2, 2, CB, 2, 2, 2, 2, 2, 2, CB, 2, 2, 2>(d_tmem, ad, bd, C::IDESC_QK, 0u);
+                    return;
+                } else if constexpr (!kTF32 && !kFP8 && C::QK_STEPS == 4) {
+                    mma4_ss_f16<2, 2, 2, 2, 2, 2>(d_tmem, ad, bd, C::IDESC_QK, 0u);
+                    return;
+                } else if constexpr (!kTF32 && !kFP8 && C::QK_STEPS == 16) {   // d = 256: two runs
+                    mma8_ss_f16<2, 2, 2, CB, 2, 2, 2, 2, 2, 2, CB, 2, 2, 2>(d_tmem, ad, bd, C::IDESC_QK, 0u);
+                    mma8_ss_f16<2, 2, 2, CB, 2, 2, 2, 2, 2, 2, CB, 2, 2, 2>(
+                        d_tmem, sdesc_adv(ad, 2 * C::CB_BYTES), sdesc_adv(bd, 2 * C::CB_BYTES),
+                        C::IDESC_QK, 1u);
+                    return;
+                }
 #pragma unroll
                 for (int kk = 0; kk < C::QK_STEPS; ++kk) {
                     const uint32_t off = (kk >> 2) * C::CB_BYTES + (kk & 3) * 32;
@@ -317,6 +333,11 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8, kTiles>::THREADS,
                 const uint32_t d_tmem = tmem + C::O_COL + D * t;
                 const uint32_t a_tmem = tmem + 128u * t;
                 const uint64_t bd = sdesc_adv(dv0, slot * C::TILE);
+                if constexpr (!kTF32 && !kFP8 && C::PV_STEPS == 8) {   // 16-bit: 8 x 16 keys
+                    mma_run_ts_f16<8, 8, C::KSTEP * 128 / 16>(d_tmem, a_tmem, bd, C::IDESC_PV,
+                                                              accumulate ? 1u : 0u);
+                    return;
+                }
 #pragma unroll
                 for (int kk = 0; kk < C::PV_STEPS; ++kk) {
                     // bf16: V as stored (MN-major); fp32: V transposed (K-major)

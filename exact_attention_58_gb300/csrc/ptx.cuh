@@ -242,6 +242,71 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
     }
 }
 
+// Runs of kind::f16 MMAs into one accumulator, each run issued from one PTX
+// block.  The MMA warp shares its SM sub-partition with busy softmax / compute
+// warps, so every instruction it issues costs several cycles; the products
+// themselves are queued in order.  The descriptors advance by adding to their
+// low 32 bits only (the 14-bit start-address field cannot carry out of them,
+// see sdesc_adv): before MMA k (k >= 1) the A and B descriptors advance by
+// A<k> and B<k> 16-byte units.  The first MMA accumulates into D when
+// first_accumulates is non-zero, every later one does.
+#define GBATTN_MMA_SS_HEAD                                                         \
+    "{\n\t.reg .pred p, pt;\n\t.reg .b32 al, ah, bl, bh;\n\t.reg .b64 a, b;\n\t" \
+    "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 pt, 0, 0;\n\t"                           \
+    "mov.b64 {al, ah}, %1;\n\tmov.b64 {bl, bh}, %2;\n\t"                          \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+#define GBATTN_MMA_SS_STEP(ia, ib)                                                      \
+    "add.u32 al, al, %" #ia ";\n\tadd.u32 bl, bl, %" #ib ";\n\t"                        \
+    "mov.b64 a, {al, ah};\n\tmov.b64 b, {bl, bh};\n\t"                                   \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+
+template <uint32_t A1, uint32_t A2, uint32_t A3, uint32_t A4, uint32_t A5, uint32_t A6, uint32_t A7,
+          uint32_t B1, uint32_t B2, uint32_t B3, uint32_t B4, uint32_t B5, uint32_t B6, uint32_t B7>
+__device__ __forceinline__ void mma8_ss_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t first_accumulates) {
+    asm volatile(GBATTN_MMA_SS_HEAD GBATTN_MMA_SS_STEP(5, 12) GBATTN_MMA_SS_STEP(6, 13)
+                     GBATTN_MMA_SS_STEP(7, 14) GBATTN_MMA_SS_STEP(8, 15) GBATTN_MMA_SS_STEP(9, 16)
+                         GBATTN_MMA_SS_STEP(10, 17) GBATTN_MMA_SS_STEP(11, 18) "}"
+                 ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(first_accumulates),
+                 "n"(A1), "n"(A2), "n"(A3), "n"(A4), "n"(A5), "n"(A6), "n"(A7),
+                 "n"(B1), "n"(B2), "n"(B3), "n"(B4), "n"(B5), "n"(B6), "n"(B7));
+}
+
+template <uint32_t A1, uint32_t A2, uint32_t A3, uint32_t B1, uint32_t B2, uint32_t B3>
+__device__ __forceinline__ void mma4_ss_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t first_accumulates) {
+    asm volatile(GBATTN_MMA_SS_HEAD GBATTN_MMA_SS_STEP(5, 8) GBATTN_MMA_SS_STEP(6, 9)
+                     GBATTN_MMA_SS_STEP(7, 10) "}"
+                 ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(first_accumulates),
+                 "n"(A1), "n"(A2), "n"(A3), "n"(B1), "n"(B2), "n"(B3));
+}
+
+// The TS form (A read from tensor memory): A advances by A_STEP columns and
+// the B descriptor by B_STEP 16-byte units per MMA; kN MMAs (4 or 8).
+#define GBATTN_MMA_TS_HEAD                                                         \
+    "{\n\t.reg .pred p, pt;\n\t.reg .b32 at, bl, bh;\n\t.reg .b64 b;\n\t"        \
+    "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 pt, 0, 0;\n\t"                           \
+    "mov.b32 at, %1;\n\tmov.b64 {bl, bh}, %2;\n\t"                                \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+#define GBATTN_MMA_TS_STEP                                                             \
+    "add.u32 at, at, %5;\n\tadd.u32 bl, bl, %6;\n\tmov.b64 b, {bl, bh};\n\t"          \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], [at], b, %3, pt;\n\t"
+
+template <int kN, uint32_t A_STEP, uint32_t B_STEP>
+__device__ __forceinline__ void mma_run_ts_f16(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t first_accumulates) {
+    static_assert(kN == 4 || kN == 8, "runs of 4 or 8 MMAs");
+    if constexpr (kN == 8)
+        asm volatile(GBATTN_MMA_TS_HEAD GBATTN_MMA_TS_STEP GBATTN_MMA_TS_STEP GBATTN_MMA_TS_STEP
+                         GBATTN_MMA_TS_STEP GBATTN_MMA_TS_STEP GBATTN_MMA_TS_STEP GBATTN_MMA_TS_STEP "}"
+                     ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(first_accumulates),
+                     "n"(A_STEP), "n"(B_STEP));
+    else
+        asm volatile(GBATTN_MMA_TS_HEAD GBATTN_MMA_TS_STEP GBATTN_MMA_TS_STEP GBATTN_MMA_TS_STEP "}"
+                     ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(first_accumulates),
+                     "n"(A_STEP), "n"(B_STEP));
+}
+
 // The same two products with 8-bit floating-point operands (kind::f8f6f4; the
 // operand formats are in the instruction descriptor).
 __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
