@@ -40,6 +40,11 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const uint16_t* __
                                                               float* __restrict__ Drow,
                                                               float* __restrict__ dq_acc, int BH,
                                                               const SeqLayout lq, int Npad) {
+    // O and LSE come from the kernel before.  The main kernel is let in only
+    // after this wait: it loads Q, K, V and dO before its own wait, and may do
+    // so only once every grid before this one has completed.
+    grid_dep_wait();
+    grid_dep_launch_dependents();
     constexpr int TPR = D / 8;                          // threads per row
     constexpr int ROWS_PER_PASS = kPreThreads / TPR;    // rows one pass of the block covers
     const int sub = threadIdx.x % TPR;                  // 8-element slice of the row
@@ -101,6 +106,8 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(uint16_t* __restric
                                                              const float* __restrict__ dq_acc,
                                                              long long n8, const SeqLayout lq,
                                                              int Npad, int D, float scale) {
+    grid_dep_launch_dependents();
+    grid_dep_wait();   // the accumulator is complete once the main kernel is
     const long long i8 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i8 >= n8) return;
     const long long e = i8 * 8;                 // element index in [BH][Npad][D]
@@ -125,9 +132,9 @@ template <int D, bool kF16>
 void launch_pre_t(unsigned grid, const void* O, const void* dO, const float* LSE, float* lse2,
                   float* Drow, float* dq_acc, int BH, const SeqLayout& lq, int Npad,
                   cudaStream_t stream) {
-    bwd_pre_kernel<D, kF16><<<grid, kPreThreads, 0, stream>>>(
-        static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), LSE, lse2, Drow, dq_acc,
-        BH, lq, Npad);
+    launch_overlapped(bwd_pre_kernel<D, kF16>, grid, kPreThreads, 0, stream,
+                      static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), LSE, lse2,
+                      Drow, dq_acc, BH, lq, Npad);
 }
 
 }  // namespace
@@ -158,12 +165,10 @@ cudaError_t launch_bwd_dq_convert(void* dQ, const float* dq_acc, int BH, const S
     const long long n8 = static_cast<long long>(BH) * Npad * d / 8;
     const unsigned grid = static_cast<unsigned>((n8 + 255) / 256);
     if (f16)
-        bwd_dq_convert_kernel<true><<<grid, 256, 0, stream>>>(static_cast<uint16_t*>(dQ), dq_acc, n8,
-                                                              lq, Npad, d, scale);
-    else
-        bwd_dq_convert_kernel<false><<<grid, 256, 0, stream>>>(static_cast<uint16_t*>(dQ), dq_acc, n8,
-                                                               lq, Npad, d, scale);
-    return cudaGetLastError();
+        return launch_overlapped(bwd_dq_convert_kernel<true>, grid, 256, 0, stream,
+                                 static_cast<uint16_t*>(dQ), dq_acc, n8, lq, Npad, d, scale);
+    return launch_overlapped(bwd_dq_convert_kernel<false>, grid, 256, 0, stream,
+                             static_cast<uint16_t*>(dQ), dq_acc, n8, lq, Npad, d, scale);
 }
 
 cudaError_t launch_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(448, 1)
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    grid_dep_launch_dependents();   // as in the d <= 128 kernel: waits before the workspace
 
     const int BH = p.B * p.H;
     int rank, bh;   // rank / 2: key block (0 = heaviest under causal), rank % 2: half of d
@@ -123,6 +124,7 @@ __global__ void __launch_bounds__(448, 1)
     const int nq = q_end - q_begin;
     const int c0 = 128 * half;   // first column of this CTA's half of d
     if (k0 >= L || nq <= 0) {    // no key of this block is attended: this half of dK, dV is 0
+        grid_dep_wait();
         const int rows = min(kTileRows, Nk - k0);
         for (int x = threadIdx.x; x < rows * 16; x += blockDim.x) {   // 16 x 8 elements a row
             const size_t e = act_offset_t<kPacked>(p.lk, bh, h, sk.start, k0 + x / 16, D) + c0 + 8 * (x % 16);
@@ -215,6 +217,7 @@ __global__ void __launch_bounds__(448, 1)
                 for (int cb = 0; cb < C::NCB; ++cb)
                     tma_load_3d(smem + C::OFF_Q + cb * C::QCB, &tmQ, full_q, cb * 64, qy, qz);
                 const size_t roff = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(qi) * QR;
+                if (it == 0) grid_dep_wait();   // LSE and D come from the preprocess
                 bulk_load(sLSE, p.lse2 + roff, QR * 4, full_q);
                 bulk_load(sD, p.Drow + roff, QR * 4, full_q);
                 ++q_issued;
@@ -486,6 +489,7 @@ __global__ void __launch_bounds__(448, 1)
         // lane = one of the 128 columns of this half; TMEM columns are the 64
         // queries of the block; each warp instruction adds 32 consecutive floats
         // of one query row.
+        grid_dep_wait();   // the accumulator is cleared by the preprocess
         const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const int dc = c0 + (warp & 3) * 32 + lane;
         for (int it = 0; it < nq; ++it) {
@@ -530,8 +534,7 @@ cudaError_t launch_bwd_d256_t(const CUtensorMap& tq, const CUtensorMap& tk, cons
     const cudaError_t e = enable_smem_per_device(kern, C::SMEM, smem_ready);
     if (e != cudaSuccess) return e;
     const unsigned grid = 2u * static_cast<unsigned>(p.nkb) * static_cast<unsigned>(p.B * p.H);
-    kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdk, tdv, p);
-    return cudaGetLastError();
+    return launch_overlapped(kern, grid, C::THREADS, C::SMEM, stream, tq, tk, tv, tdo, tdk, tdv, p);
 }
 
 template <bool kF16, bool kPacked, bool kWindow>

@@ -105,6 +105,10 @@ __global__ void __launch_bounds__(448, 1)
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // Launched overlapped with the preprocess: K, V, Q and dO (inputs) load
+    // while it finishes; the workspace it writes (LSE, D, the cleared dQ
+    // accumulator) and the outputs are touched only after grid_dep_wait().
+    grid_dep_launch_dependents();
 
     const int BH = p.B * p.H;
     int kb, bh;   // causal: key block 0 meets every query block, so rank 0 is heaviest
@@ -141,6 +145,7 @@ __global__ void __launch_bounds__(448, 1)
     }
     const int nq = q_end - q_begin;
     if (k0 >= L || nq <= 0) {   // no key of this block is attended: dK = dV = 0
+        grid_dep_wait();
         const int rows = min(kTileRows, Nk - k0);
         constexpr int kRow16 = D / 8;   // uint4 per row
         for (int x = threadIdx.x; x < rows * kRow16; x += blockDim.x) {
@@ -229,6 +234,7 @@ __global__ void __launch_bounds__(448, 1)
                                 &full_q[stage], cb * 64, qy, qz);
                 }
                 const size_t roff = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(qi) * kTileRows;
+                if (it == 0) grid_dep_wait();   // LSE and D come from the preprocess
                 bulk_load(sLSE + stage * kTileRows, p.lse2 + roff, 512, &full_q[stage]);
                 bulk_load(sD + stage * kTileRows, p.Drow + roff, 512, &full_q[stage]);
                 ++issued;
@@ -604,6 +610,7 @@ __global__ void __launch_bounds__(448, 1)
         }
     } else {
         // ================= dQ: read dQ out of TMEM, add into the workspace =================
+        grid_dep_wait();   // the accumulator is cleared by the preprocess
         const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         for (int it = 0; it < nq; ++it) {
             const size_t row0 = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(q_begin + it) * kTileRows;
@@ -690,8 +697,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     const cudaError_t e = enable_smem_per_device(kern, C::SMEM, smem_ready);
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(p.nkb) * static_cast<unsigned>(p.B * p.H);
-    kern<<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, tv, tdo, tdk, tdv, p);
-    return cudaGetLastError();
+    return launch_overlapped(kern, grid, C::THREADS, C::SMEM, stream, tq, tk, tv, tdo, tdk, tdv, p);
 }
 
 template <int D, bool kF16, bool kPacked, bool kWindow>

@@ -6,6 +6,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <utility>
 
 #include "gbattn.h"
 
@@ -83,6 +84,25 @@ cudaError_t enable_smem_per_device(Kernel kern, int bytes, std::atomic<unsigned 
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
     return e;
+}
+
+// Launch on `stream` with programmatic stream serialization, so that the
+// kernel's CTAs may start (and run up to their grid_dep_wait()) while the
+// kernel before it finishes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // Tensor map over a contiguous [B*H][N][d] array, boxes of `rows` rows (128

@@ -138,6 +138,21 @@ __device__ __forceinline__ void bulk_wait_group_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream is still
+// running (once that one has signalled launch_dependents); grid_dep_wait()
+// then blocks the calling thread until the preceding grid has completed and
+// its memory operations are visible.  Every kernel here calls it before its
+// first access to memory a preceding kernel may still write or read.  Only
+// the backward's main kernel reads anything (its inputs) before that wait, so
+// the preprocess launched just before it signals its dependents after its own
+// wait; the main and dQ-conversion kernels signal at their start, the forward
+// not at all.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Barrier over `nthreads` threads (a multiple of 32) on hardware barrier `id`
 // (1-15; 0 is the one __syncthreads uses).
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {

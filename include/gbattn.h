@@ -66,7 +66,13 @@
  *             library never allocates, frees or synchronises.
  *  Streams    stream is a cudaStream_t (NULL = the legacy default stream).
  *             Work is enqueued asynchronously; outputs are valid once the
- *             stream has reached the work.
+ *             stream has reached the work.  Kernels are launched with
+ *             programmatic stream serialization: a kernel's blocks may be
+ *             resident before the work ahead of it in the stream has
+ *             finished, but no kernel touches a buffer before every earlier
+ *             piece of work that may use it has finished (griddepcontrol
+ *             .wait); the three backward stages overlap one another's
+ *             start-up.
  *  Errors     Argument errors are returned before anything is enqueued, with
  *             the outputs untouched.  A failed launch returns ATTN_ERR_CUDA.
  *             Errors detected on the device (a bounded wait that expired, an
