@@ -1,7 +1,7 @@
 // attn_bwd.cu — backward of the fused exact attention for sm_103a.
 //
 // Three launches:
-//   preprocess  D_i = dO_i . O_i, LSE_i * log2(e) into a padded workspace,
+//   preprocess  D_i = dO_i . O_i, -LSE_i * log2(e) into a padded workspace,
 //               and a cleared fp32 dQ accumulator;
 //   main        one CTA per (head, 128-key block): recomputes P tile by tile
 //               from Q, K and the stored log-sum-exp (the recomputation of
@@ -18,10 +18,10 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// D_i = dO_i . O_i and lse2_i = LSE_i log2(e) for every padded row, and the
+// D_i = dO_i . O_i and lse2_i = -LSE_i log2(e) for every padded row, and the
 // row's fp32 dQ accumulator cleared.  Rows past the sequence's end (and rows
-// whose LSE is -inf, which have no valid key) get lse2 = +inf so that the
-// main kernel's P = exp2(s - lse2) is exactly 0 there; for packed sequences
+// whose LSE is -inf, which have no valid key) get lse2 = -inf so that the
+// main kernel's P = exp2(s + lse2) is exactly 0 there; for packed sequences
 // this also cancels the next sequence's rows that a tile load brings in.
 // The workspace is [B*H][Npad] rows whatever the placement of O, dO, LSE.
 //
@@ -88,19 +88,25 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const uint16_t* __
             const int row = static_cast<int>(prow[k] % Npad);
             int h;
             const SeqSpan sq = seq_span_bh(lq, bh, h);
-            float l2 = INFINITY;
+            float nl2 = -INFINITY;   // -LSE log2e; -inf: the row takes no part
             if (row < sq.len) {
                 const float lse = LSE[rowval_offset(lq, bh, h, sq.start, row)];
-                if (lse != -INFINITY) l2 = lse * kLog2e;
+                if (lse != -INFINITY) nl2 = -lse * kLog2e;
             }
-            lse2[prow[k]] = l2;
+            lse2[prow[k]] = nl2;
             Drow[prow[k]] = acc;
         }
     }
 }
 
-// dQ = scale * acc for the rows of every sequence; 8 elements (two 16-byte
-// loads, one 16-byte store) per thread, walking the [B*H][Npad][D] workspace.
+// dQ = scale * acc for the rows of every sequence, walking the
+// [B*H][Npad][D] workspace in groups of 8 elements (two 16-byte loads, one
+// 16-byte store).  A thread takes kConvGroups groups 256 groups apart (each
+// warp access stays one contiguous kilobyte) and issues all their loads
+// before the first store, so that enough bytes are in flight; the workspace
+// is read once, with the evict-first hint.
+constexpr int kConvGroups = 4;
+
 template <bool kF16>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(uint16_t* __restrict__ dQ,
                                                              const float* __restrict__ dq_acc,
@@ -108,24 +114,36 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(uint16_t* __restric
                                                              int Npad, int D, float scale) {
     grid_dep_launch_dependents();
     grid_dep_wait();   // the accumulator is complete once the main kernel is
-    const long long i8 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i8 >= n8) return;
-    const long long e = i8 * 8;                 // element index in [BH][Npad][D]
-    const long long rowg = e / D;               // bh * Npad + row
-    const int c = static_cast<int>(e % D);
-    const int bh = static_cast<int>(rowg / Npad);
-    const int row = static_cast<int>(rowg % Npad);
-    int h;
-    const SeqSpan sq = seq_span_bh(lq, bh, h);
-    if (row >= sq.len) return;
-    const float4* src = reinterpret_cast<const float4*>(dq_acc + e);
-    const float4 x = src[0], y = src[1];
-    uint4 out;
-    out.x = pack_h2<kF16>(x.x * scale, x.y * scale);
-    out.y = pack_h2<kF16>(x.z * scale, x.w * scale);
-    out.z = pack_h2<kF16>(y.x * scale, y.y * scale);
-    out.w = pack_h2<kF16>(y.z * scale, y.w * scale);
-    *reinterpret_cast<uint4*>(dQ + act_offset(lq, bh, h, sq.start, row, D) + c) = out;
+    const long long g0 = static_cast<long long>(blockIdx.x) * (256 * kConvGroups) + threadIdx.x;
+    float4 x[kConvGroups], y[kConvGroups];
+#pragma unroll
+    for (int u = 0; u < kConvGroups; ++u) {
+        const long long i8 = g0 + 256 * u;
+        if (i8 < n8) {
+            const float4* src = reinterpret_cast<const float4*>(dq_acc + i8 * 8);
+            x[u] = __ldcs(src);
+            y[u] = __ldcs(src + 1);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kConvGroups; ++u) {
+        const long long i8 = g0 + 256 * u;
+        if (i8 >= n8) break;
+        const long long e = i8 * 8;                 // element index in [BH][Npad][D]
+        const long long rowg = e / D;               // bh * Npad + row
+        const int c = static_cast<int>(e % D);
+        const int bh = static_cast<int>(rowg / Npad);
+        const int row = static_cast<int>(rowg % Npad);
+        int h;
+        const SeqSpan sq = seq_span_bh(lq, bh, h);
+        if (row >= sq.len) continue;
+        uint4 out;
+        out.x = pack_h2<kF16>(x[u].x * scale, x[u].y * scale);
+        out.y = pack_h2<kF16>(x[u].z * scale, x[u].w * scale);
+        out.z = pack_h2<kF16>(y[u].x * scale, y[u].y * scale);
+        out.w = pack_h2<kF16>(y[u].z * scale, y[u].w * scale);
+        *reinterpret_cast<uint4*>(dQ + act_offset(lq, bh, h, sq.start, row, D) + c) = out;
+    }
 }
 
 template <int D, bool kF16>
@@ -163,7 +181,7 @@ cudaError_t launch_bwd_pre(const void* O, const void* dO, const float* LSE, floa
 cudaError_t launch_bwd_dq_convert(void* dQ, const float* dq_acc, int BH, const SeqLayout& lq,
                                   int Npad, int d, bool f16, float scale, cudaStream_t stream) {
     const long long n8 = static_cast<long long>(BH) * Npad * d / 8;
-    const unsigned grid = static_cast<unsigned>((n8 + 255) / 256);
+    const unsigned grid = static_cast<unsigned>((n8 + 256 * kConvGroups - 1) / (256 * kConvGroups));
     if (f16)
         return launch_overlapped(bwd_dq_convert_kernel<true>, grid, 256, 0, stream,
                                  static_cast<uint16_t*>(dQ), dq_acc, n8, lq, Npad, d, scale);

@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int col = 16 * c + 2 * e + u;
-                        float x = ex2_approx(fmaf(__uint_as_float(sv[col]), p.scale_log2, -lse_s[col]));
+                        float x = ex2_approx(fmaf(__uint_as_float(sv[col]), p.scale_log2, lse_s[col]));
                         const int iq = q0h + col;
                         const bool valid = row_valid && (!diag || jo <= iq) &&
                                            (!wmask || (iq - jo < W && (kCausal || jo - iq < W)));

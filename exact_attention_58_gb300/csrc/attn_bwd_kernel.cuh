@@ -4,6 +4,8 @@
 
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "philox.cuh"
 #include "ptx.cuh"
@@ -403,6 +405,7 @@ __global__ void __launch_bounds__(448, 1)
         const uint32_t tS = tl + C::C_S + 64 * hh;
         const uint32_t tdP = tl + C::C_DP + 64 * hh;   // this half's dP^T columns
         const bool row_valid = j < L;
+        const bool warp_has_invalid_row = __any_sync(0xffffffffu, !row_valid);
         const int jo = j - off;   // this key's position on the query axis
         uint8_t* rowp = smem + C::OFF_DS + hh * C::CB_BYTES + r * 128;
         bool ok = true;
@@ -426,74 +429,92 @@ __global__ void __launch_bounds__(448, 1)
                                          (!kCausal && k0 + kTileRows - 1 - qi * kTileRows - off >= W));
             // ---- phase 1 (while dP^T is still on the tensor pipe): P from S ----
             // 16-column chunks; the next chunk's TMEM load overlaps this chunk's
-            // math.  P (undropped, fp32) stays in registers for phase 2.
+            // math.  P (undropped, fp32) stays in registers for phase 2.  The
+            // exponents scale s - LSE log2e are formed two columns per
+            // instruction; blocks without a masked pair take a copy of the loop
+            // with no mask tests.
             float pr[64];
             uint32_t keepw[4];
             uint32_t buf[2][16];
-            tmem_ld16(tS, buf[0]);
-            tmem_ld_wait();
-            reg_fence(buf[0]);
+            const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
+            auto phase1 = [&](auto masked_tag) {
+                constexpr bool kMasked = decltype(masked_tag)::value;
+                tmem_ld16(tS, buf[0]);
+                tmem_ld_wait();
+                reg_fence(buf[0]);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (c < 3) tmem_ld16(tS + 16 * (c + 1), buf[(c + 1) & 1]);
-                const uint32_t* sv = buf[c & 1];
-                uint32_t keep = 0xFFFFu;   // bit e: column 16c+e of this half kept
-                if constexpr (kDropout) {
-                    // Lanes 4m..4m+3 own keys 4m..4m+3 of one Philox counter
-                    // (i, j>>2, h, b): lane a draws the words of query 4g+a and
-                    // the quad swaps bits so each lane gets its own key's bits.
-                    keep = 0u;
-                    const int a = lane & 3;
+                for (int c = 0; c < 4; ++c) {
+                    if (c < 3) tmem_ld16(tS + 16 * (c + 1), buf[(c + 1) & 1]);
+                    const uint32_t* sv = buf[c & 1];
+                    uint32_t keep = 0xFFFFu;   // bit e: column 16c+e of this half kept
+                    if constexpr (kDropout) {
+                        // Lanes 4m..4m+3 own keys 4m..4m+3 of one Philox counter
+                        // (i, j>>2, h, b): lane a draws the words of query 4g+a and
+                        // the quad swaps bits so each lane gets its own key's bits.
+                        keep = 0u;
+                        const int a = lane & 3;
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const int iq = q0h + 16 * c + 4 * g + a;
-                        uint32_t v = dropout_keep4(p.seed_lo, p.seed_hi, p.drop_threshold, iq,
-                                                   j & ~3, h, b)
-                                     << (4 * a);
-                        v |= __shfl_xor_sync(0xffffffffu, v, 1);
-                        v |= __shfl_xor_sync(0xffffffffu, v, 2);
-                        const int e = lane & 3;   // this thread's key within the quad
+                        for (int g = 0; g < 4; ++g) {
+                            const int iq = q0h + 16 * c + 4 * g + a;
+                            uint32_t v = dropout_keep4(p.seed_lo, p.seed_hi, p.drop_threshold, iq,
+                                                       j & ~3, h, b)
+                                         << (4 * a);
+                            v |= __shfl_xor_sync(0xffffffffu, v, 1);
+                            v |= __shfl_xor_sync(0xffffffffu, v, 2);
+                            const int e = lane & 3;   // this thread's key within the quad
 #pragma unroll
-                        for (int a2 = 0; a2 < 4; ++a2)
-                            keep |= ((v >> (4 * a2 + e)) & 1u) << (4 * g + a2);
+                            for (int a2 = 0; a2 < 4; ++a2)
+                                keep |= ((v >> (4 * a2 + e)) & 1u) << (4 * g + a2);
+                        }
+                    }
+                    keepw[c] = keep;
+                    float nl[16];   // this chunk's -LSE log2e values, four 16-byte shared loads
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const float4 t4 = reinterpret_cast<const float4*>(lse_s + 16 * c)[v];
+                        nl[4 * v] = t4.x;
+                        nl[4 * v + 1] = t4.y;
+                        nl[4 * v + 2] = t4.z;
+                        nl[4 * v + 3] = t4.w;
+                    }
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int col = 16 * c + 2 * e;
+                        float x[2];
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])),
+                                         scale2, f2_pack(nl[2 * e], nl[2 * e + 1])),
+                                  x[0], x[1]);
+                        float pd[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            x[u] = ex2_approx(x[u]);
+                            if constexpr (kMasked) {
+                                const int iq = q0h + col + u;   // query index
+                                const bool valid = row_valid && (!diag || jo <= iq) &&
+                                                   (!wmask || (iq - jo < W && (kCausal || jo - iq < W)));
+                                x[u] = valid ? x[u] : 0.f;
+                            }
+                            pr[col + u] = x[u];
+                            pd[u] = x[u];
+                            if constexpr (kDropout)
+                                pd[u] = ((keep >> (2 * e + u)) & 1u) ? x[u] * p.drop_scale : 0.f;
+                        }
+                        pk[e] = pack_h2<kF16>(pd[0], pd[1]);
+                    }
+                    tmem_st8(tS + 8 * c, pk);
+                    if (c < 3) {
+                        tmem_ld_wait();
+                        reg_fence(buf[(c + 1) & 1]);
                     }
                 }
-                keepw[c] = keep;
-                float lv[16];   // this chunk's LSE values, four 16-byte shared loads
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const float4 t4 = reinterpret_cast<const float4*>(lse_s + 16 * c)[v];
-                    lv[4 * v] = t4.x;
-                    lv[4 * v + 1] = t4.y;
-                    lv[4 * v + 2] = t4.z;
-                    lv[4 * v + 3] = t4.w;
-                }
-                uint32_t pk[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float pd[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int col = 16 * c + 2 * e + u;
-                        float x = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), p.scale_log2,
-                                                  -lv[2 * e + u]));
-                        const int iq = q0h + col;   // query index
-                        const bool valid = row_valid && (!diag || jo <= iq) &&
-                                           (!wmask || (iq - jo < W && (kCausal || jo - iq < W)));
-                        x = valid ? x : 0.f;
-                        pr[col] = x;
-                        pd[u] = x;
-                        if constexpr (kDropout)
-                            pd[u] = ((keep >> (2 * e + u)) & 1u) ? x * p.drop_scale : 0.f;
-                    }
-                    pk[e] = pack_h2<kF16>(pd[0], pd[1]);
-                }
-                tmem_st8(tS + 8 * c, pk);
-                if (c < 3) {
-                    tmem_ld_wait();
-                    reg_fence(buf[(c + 1) & 1]);
-                }
-            }
+            };
+            // The choice must be the same in all 32 lanes: the tensor-memory
+            // loads and stores and the shuffles inside are warp-collective.
+            if (diag || wmask || warp_has_invalid_row)
+                phase1(std::true_type{});
+            else
+                phase1(std::false_type{});
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bar_P[hh]);
@@ -522,16 +543,19 @@ __global__ void __launch_bounds__(448, 1)
                 }
                 uint32_t dk[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float ds[2];
+                for (int e = 0; e < 8; ++e) {   // two columns per instruction
+                    const int col = 16 * c + 2 * e;
+                    float dp[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const int col = 16 * c + 2 * e + u;
-                        float dp = __uint_as_float(dpv[2 * e + u]);
+                        dp[u] = __uint_as_float(dpv[2 * e + u]);
                         if constexpr (kDropout)
-                            dp = ((keepw[c] >> (2 * e + u)) & 1u) ? dp * p.drop_scale : 0.f;
-                        ds[u] = pr[col] * (dp - dv[2 * e + u]);
+                            dp[u] = ((keepw[c] >> (2 * e + u)) & 1u) ? dp[u] * p.drop_scale : 0.f;
                     }
+                    float ds[2];
+                    f2_unpack(f2_mul(f2_pack(pr[col], pr[col + 1]),
+                                     f2_sub(f2_pack(dp[0], dp[1]), f2_pack(dv[2 * e], dv[2 * e + 1]))),
+                              ds[0], ds[1]);
                     dk[e] = pack_h2<kF16>(ds[0], ds[1]);
                 }
                 // dS (bf16) into shared memory: query index innermost (one

@@ -55,7 +55,7 @@ struct BwdParams {
     const int32_t* key_lens;
     int* dev_status;
     float* dq_acc;            // [B*H][Npad][d] fp32
-    const float* lse2;        // [B*H][Npad] LSE * log2(e); +inf marks "no contribution"
+    const float* lse2;        // [B*H][Npad] -LSE * log2(e); -inf marks "no contribution"
     const float* Drow;        // [B*H][Npad] dO . O
     int B, H, N, Npad;        // N: query rows, Npad: N rounded up to 128
     int Nk;                   // keys

@@ -163,7 +163,7 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
  * The three stages of attn_bwd, exported so that a caller can enqueue (and
  * time) them one by one.  Same arguments and rules as attn_bwd; calling the
  * three in this order on one stream with one workspace is exactly attn_bwd.
- *   preprocess: D_i = dO_i . O_i and LSE_i * log2(e) into the workspace;
+ *   preprocess: D_i = dO_i . O_i and -LSE_i * log2(e) into the workspace;
  *               clears the dQ accumulator.
  *   main:       recomputes P tile by tile; writes dK, dV; accumulates dQ
  *               (unscaled) into the workspace.
