@@ -189,6 +189,65 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # the float64 oracle on the host cores (a bounded sample of the same workload)
 # ---------------------------------------------------------------------------
+def tmap_encode_us(ptr: int, BH: int, N: int, d: int, reps: int = 20000) -> float:
+    """Host time of one cuTensorMapEncodeTiled call of the kind every entry
+    point makes per tensor ([B*H, N, d] 16-bit, 128-byte swizzle, 64 x 128
+    box), less the cost of a trivial call through the same ctypes path."""
+    import ctypes
+    drv = ctypes.CDLL("libcuda.so.1")
+    enc = drv.cuTensorMapEncodeTiled
+    enc.restype = ctypes.c_int
+    u64, u32 = ctypes.c_uint64, ctypes.c_uint32
+    tmap = (u64 * 16)()
+    dims, strides = (u64 * 3)(d, N, BH), (u64 * 2)(d * 2, N * d * 2)
+    box, estr = (u32 * 3)(64, 128, 1), (u32 * 3)(1, 1, 1)
+    # data type bf16 (9), 3-D, no interleave, 128-byte swizzle (3), L2 256B (3), no OOB NaN
+    call = (tmap, 9, 3, ctypes.c_void_p(ptr), dims, strides, box, estr, 0, 3, 3, 0)
+    if enc(*call) != 0:
+        return float("nan")
+    noop = drv.cuDriverGetVersion
+    ver = ctypes.c_int()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        enc(*call)
+    t1 = time.perf_counter()
+    for _ in range(reps):
+        noop(ctypes.byref(ver))
+    t2 = time.perf_counter()
+    return max(0.0, ((t1 - t0) - (t2 - t1)) / reps * 1e6)
+
+
+def pinned_copy_gbs(host: list, dev: list, stream, reps: int = 5) -> dict:
+    """Raw copy rates between pinned host buffers and device buffers: each
+    direction alone, then both at once on two streams."""
+    import torch
+    other = torch.cuda.Stream()
+    nbytes = sum(t.numel() * t.element_size() for t in host)
+
+    def timed(fn_h2d, fn_d2h):
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        best = float("inf")
+        for _ in range(reps):
+            s.record(stream)
+            other.wait_event(s)
+            for t_h, t_d in zip(host, dev):
+                if fn_h2d:
+                    with torch.cuda.stream(stream):
+                        t_d.copy_(t_h, non_blocking=True)
+                if fn_d2h:
+                    with torch.cuda.stream(other):
+                        t_h.copy_(t_d, non_blocking=True)
+            stream.wait_stream(other)
+            e.record(stream)
+            torch.cuda.synchronize()
+            best = min(best, s.elapsed_time(e))
+        return nbytes * (int(fn_h2d) + int(fn_d2h)) / (best * 1e-3) / 1e9
+
+    return {"h2d": round(timed(True, False), 1), "d2h": round(timed(False, True), 1),
+            "both_ways_total": round(timed(True, True), 1), "bytes": nbytes}
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -539,10 +598,26 @@ def run_ours(args, w: Workload):
         e_ms = s_ev.elapsed_time(e_ev)
         h2d_bytes = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h_bytes = sum(t.numel() * t.element_size() for t in host_out.values())
+        # host side: the time to enqueue one step's public calls (argument
+        # checks, tensor-map encodes, launches), one tensor-map encode, and the
+        # raw pinned copy rates the pipeline is bounded by
+        reps = 50
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            api(slots[0], comp)
+        api_us = (time.perf_counter() - t0) / reps * 1e6
+        torch.cuda.synchronize()
+        pairs = [(host_in[n], slots[1][n]) for n in host_in]
+        pairs += [(host_out[n], slots[1][n]) for n in out_names]
+        copy_gbs = pinned_copy_gbs([h for h, _ in pairs], [dv for _, dv in pairs], h2d)
         e2e = {"value": flops_step * args.e2e_steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
                "ms_per_step": e_ms / args.e2e_steps,
-               "pipeline": "2 buffer sets; copies in, compute, copies out on three streams"}
+               "pipeline": "2 buffer sets; copies in, compute, copies out on three streams",
+               "host_enqueue_us_per_step": round(api_us, 1),
+               "tmap_encode_us": round(tmap_encode_us(q.data_ptr(), w.B * w.H, w.N, w.d), 3)
+               if lens is None and w.d <= 256 else None,
+               "raw_pinned_copy_gbs": copy_gbs}
 
     cpu = None
     # the sample is forward+backward of the default (unwindowed) configuration
