@@ -133,6 +133,14 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8, kTiles>::THREADS,
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (C::TILES + C::NSLOT) * C::TILE);
     uint64_t* bar_q = bars;               // [2] one per query tile
     uint64_t* full = bars + 2;
+    // Ring slots are freed by tensor-pipe commits.  A ring of kPairs >= 2 K/V
+    // pairs takes one commit per key block j (after its last S, so K_j and
+    // V_{j-1} are both read) on empty[(j - jbeg) % kPairs]: one commit fewer per
+    // block than a commit per slot, and each commit costs the MMA warp a
+    // queue slot (an extra one was 0.85% slower at C3).  A one-pair ring keeps
+    // a barrier per slot.
+    constexpr int kPairs = C::NSLOT / 2;
+    constexpr bool kBlockRelease = kPairs >= 2;
     uint64_t* empty = full + C::NSLOT;
     uint64_t* bar_s = empty + C::NSLOT;   // [2]
     uint64_t* bar_p = bar_s + 2;          // [2]
@@ -271,7 +279,19 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8, kTiles>::THREADS,
                     }
                     const int slot = seq % C::NSLOT;
                     const uint32_t ph = (seq / C::NSLOT) & 1;
-                    if (!mbar_wait_warp(&empty[slot], ph ^ 1, s_abort, lim)) {
+                    bool free_ok;
+                    if constexpr (kBlockRelease) {
+                        // the slot's previous tile (K or V of block bi - P) is
+                        // free once block bi - P (K) or bi - P + 1 (V) has
+                        // released its pair
+                        const int bi = j - jbeg;
+                        const int wb = which == 0 ? bi - kPairs : bi - kPairs + 1;
+                        free_ok = bi < kPairs ||
+                                  mbar_wait_warp(&empty[wb % kPairs], (wb / kPairs) & 1, s_abort, lim);
+                    } else {
+                        free_ok = mbar_wait_warp(&empty[slot], ph ^ 1, s_abort, lim);
+                    }
+                    if (!free_ok) {
                         ok = false;
                         break;
                     }
@@ -434,8 +454,12 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8, kTiles>::THREADS,
                     }
                 }
                 if (!ok) break;
-                tc_commit(&empty[kslot]);
-                if (j > jbeg && v_last < 0) tc_commit(&empty[v_slot]);   // unless released above
+                if constexpr (kBlockRelease) {
+                    tc_commit(&empty[(j - jbeg) % kPairs]);
+                } else {
+                    tc_commit(&empty[kslot]);
+                    if (j > jbeg && v_last < 0) tc_commit(&empty[v_slot]);   // unless released above
+                }
                 v_slot = next_v_slot;
                 v_phase = next_v_phase;
                 v_ready = false;
