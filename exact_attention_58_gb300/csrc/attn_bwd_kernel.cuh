@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(448, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* bar_kv = bars + 0;
     uint64_t* full_q = bars + 1;      // [2]
-    uint64_t* empty_q = bars + 3;     // [2]
+    // bars + 3, bars + 4: unused (a Q/dO stage is released by bar_dP[0])
     uint64_t* bar_S = bars + 5;       // S^T in TMEM
     uint64_t* bar_P = bars + 6;       // [2] P of a query half in TMEM (one per warpgroup)
     uint64_t* bar_dQ = bars + 8;       // [2] dQ (d = 128: each query half of dQ^T) in TMEM
@@ -184,7 +184,6 @@ __global__ void __launch_bounds__(448, 1)
         mbar_init(bar_kv, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&full_q[s], 1);
-            mbar_init(&empty_q[s], 1);
             mbar_init(&bar_P[s], kTileRows);
             mbar_init(&bar_dS[s], kTileRows);
             mbar_init(&bar_dP[s], 1);
@@ -223,8 +222,15 @@ __global__ void __launch_bounds__(448, 1)
             int issued = 0;
             for (int it = 0; it < nq; ++it) {
                 const int stage = it & 1;
-                const uint32_t ph = (it >> 1) & 1;
-                if (!mbar_wait(&empty_q[stage], ph ^ 1, s_abort)) break;
+                // The stage's previous block (it - 2) is done with it once dK of
+                // that block has run, which the commit of the next dP^T half 0
+                // (dP of block it - 1, completion it - 1 of bar_dP[0]) covers:
+                // the MMA warp spends no commit of its own on the release.
+                // (A parity wait must name the phase in progress or the one just
+                // completed: block 2 first waits for completion 0, after which
+                // each block's wait is at most one phase ahead of the last.)
+                if (it == 2 && !mbar_wait(&bar_dP[0], 0, s_abort)) break;
+                if (it >= 2 && !mbar_wait(&bar_dP[0], (it - 1) & 1, s_abort)) break;
                 const int qi = q_begin + it;
                 mbar_arrive_expect_tx(&full_q[stage], 2 * C::TILE + 1024);
                 int qy, qz;
@@ -381,7 +387,6 @@ __global__ void __launch_bounds__(448, 1)
                     issue_dq_half(1);
                 }
                 issue_dk_half(1, q_mn, false);   // runs while the dQ warps drain dQ
-                tc_commit(&empty_q[stage]);
                 if (more) {
                     // dP^T of the next block.  Its commits also cover dK and dQ
                     // of this block: when they fire, the dS buffer is free.
