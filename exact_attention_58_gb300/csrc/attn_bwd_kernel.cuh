@@ -305,9 +305,18 @@ __global__ void __launch_bounds__(448, 1)
                     mma4_ss_f16<2, 2, 2, 2, 2, 2>(tmem + C::C_DP + 64 * hh, dV_k, do_k,
                                                   C::IDESC_DP_HALF, 0u);
             };
-            // d = 128: the next dP^T half may only land once the dQ warps have
-            // read the dQ^T half that shares its columns.
+            // dP^T of block it_prev + 1, half by half.  d = 128: the next dP^T
+            // half may only land once the dQ warps have read the dQ^T half that
+            // shares its columns, and P of a half is usually in before that, so
+            // each dP^T half is followed by the block's dV += P^T dO for the
+            // same query half, which fills the tensor pipe while the dQ warps
+            // drain dQ (0.9% faster at C3).  d = 64 has no such wait, and there
+            // dV goes at the top of the block's iteration (interleaving it
+            // delayed the second dP^T half: 5% slower at C5).
+            constexpr bool kDvInDp = D == 128;
             auto issue_dp = [&](int stage, int it_prev) {
+                const int itb = it_prev + 1;
+                const uint64_t do_mn = sdesc_adv(dO_mn0, stage * C::TILE);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     if (D == 128 && it_prev >= 0 &&
@@ -316,14 +325,20 @@ __global__ void __launch_bounds__(448, 1)
                     tc_fence_after();
                     issue_dp_half(stage, hh);
                     tc_commit(&bar_dP[hh]);
+                    if constexpr (kDvInDp) {
+                        if (!mbar_wait(&bar_P[hh], itb & 1, s_abort)) return false;
+                        tc_fence_after();
+                        issue_dv_half(hh, do_mn, itb == 0 && hh == 0);
+                    }
                 }
                 return true;
             };
             // Software pipeline over query blocks: S^T of block i+1 is issued
             // behind dV of block i (the tensor pipe runs one thread's MMAs in
             // issue order, so it reads P_i before S^T_{i+1} overwrites it), and
-            // dP^T of block i+1 right behind dQ and dK of block i.  The compute
-            // warps then find the next S^T on its way while they build dS.
+            // dP^T of block i+1 right behind dQ and dK of block i, each half of
+            // it followed by dV of block i+1 for that half.  The compute warps
+            // then find the next S^T on its way while they build dS.
             bool ok = mbar_wait(bar_kv, 0, s_abort) && mbar_wait(&full_q[0], 0, s_abort);
             if (ok) {
                 tc_fence_after();
@@ -336,15 +351,17 @@ __global__ void __launch_bounds__(448, 1)
                 const bool more = it + 1 < nq;
                 const int nstage = stage ^ 1;
                 const uint64_t q_mn = sdesc_adv(dQ_mn0, stage * C::TILE);
-                const uint64_t do_mn = sdesc_adv(dO_mn0, stage * C::TILE);
+                if constexpr (!kDvInDp) {
+                    const uint64_t do_mn = sdesc_adv(dO_mn0, stage * C::TILE);
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {   // dV += P^T dO as soon as each half of P is in
-                    ok = mbar_wait(&bar_P[hh], it & 1, s_abort);
+                    for (int hh = 0; hh < 2; ++hh) {   // dV += P^T dO as each half of P is in
+                        ok = mbar_wait(&bar_P[hh], it & 1, s_abort);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_dv_half(hh, do_mn, it == 0 && hh == 0);
+                    }
                     if (!ok) break;
-                    tc_fence_after();
-                    issue_dv_half(hh, do_mn, it == 0 && hh == 0);
                 }
-                if (!ok) break;
                 auto issue_next_s = [&]() {
                     ok = mbar_wait(&full_q[nstage], ((it + 1) >> 1) & 1, s_abort);
                     if (!ok) return;
