@@ -310,13 +310,26 @@ __global__ void __launch_bounds__(448, 1)
             // shares its columns, and P of a half is usually in before that, so
             // each dP^T half is followed by the block's dV += P^T dO for the
             // same query half, which fills the tensor pipe while the dQ warps
-            // drain dQ (0.9% faster at C3).  d = 64 has no such wait, and there
-            // dV goes at the top of the block's iteration (interleaving it
-            // delayed the second dP^T half: 5% slower at C5).
+            // drain dQ (0.9% faster at C3, 1% slower with 512- and 1024-key
+            // windows, whose CTAs walk few blocks; testing for P without
+            // waiting and otherwise leaving dV for the top of the iteration was
+            // 1% slower at C3).  d = 64 has no such wait, and there dV goes at
+            // the top of the block's iteration (interleaving it delayed the
+            // second dP^T half: 5% slower at C5).
             constexpr bool kDvInDp = D == 128;
             auto issue_dp = [&](int stage, int it_prev) {
                 const int itb = it_prev + 1;
                 const uint64_t do_mn = sdesc_adv(dO_mn0, stage * C::TILE);
+                auto issue_dv = [&](int hh) {
+                    if (!mbar_wait(&bar_P[hh], itb & 1, s_abort)) return false;
+                    tc_fence_after();
+                    issue_dv_half(hh, do_mn, itb == 0 && hh == 0);
+                    return true;
+                };
+                // A CTA's first block has no dQ^T to wait for: both its dP^T
+                // halves go at once (the start-up is on the critical path), dV
+                // after them.
+                const bool interleave = kDvInDp && it_prev >= 0;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     if (D == 128 && it_prev >= 0 &&
@@ -325,12 +338,11 @@ __global__ void __launch_bounds__(448, 1)
                     tc_fence_after();
                     issue_dp_half(stage, hh);
                     tc_commit(&bar_dP[hh]);
-                    if constexpr (kDvInDp) {
-                        if (!mbar_wait(&bar_P[hh], itb & 1, s_abort)) return false;
-                        tc_fence_after();
-                        issue_dv_half(hh, do_mn, itb == 0 && hh == 0);
-                    }
+                    if (interleave && !issue_dv(hh)) return false;
                 }
+                if (kDvInDp && !interleave)
+                    for (int hh = 0; hh < 2; ++hh)
+                        if (!issue_dv(hh)) return false;
                 return true;
             };
             // Software pipeline over query blocks: S^T of block i+1 is issued
