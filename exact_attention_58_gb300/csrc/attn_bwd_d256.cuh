@@ -244,6 +244,15 @@ __global__ void __launch_bounds__(448, 1)
             const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + C::OFF_K + 2 * half * C::KCB), C::KCB, 1024);
             const uint64_t dS_mn = sdesc_sw128(smem_u32(smem + C::OFF_DS), C::QCB, 1024);
             const uint64_t dS_k = sdesc_sw128(smem_u32(smem + C::OFF_DS), 16, 1024);   // keys as rows
+            // Each group of MMAs goes out as runs of inline PTX (ptx.cuh) whose
+            // descriptors advance by constants: 32 bytes per K step inside a
+            // 128-byte column block, then on to the next column block.
+            constexpr uint32_t KJ = C::KCB / 16 - 6, QJ = C::QCB / 16 - 6;
+            auto issue_full_d = [&](uint32_t d_tmem, uint64_t a_k, uint64_t b_k) {   // K = 256
+                mma8_ss_f16<2, 2, 2, KJ, 2, 2, 2, 2, 2, 2, QJ, 2, 2, 2>(d_tmem, a_k, b_k, C::IDESC_SDP, 0u);
+                mma8_ss_f16<2, 2, 2, KJ, 2, 2, 2, 2, 2, 2, QJ, 2, 2, 2>(
+                    d_tmem, sdesc_adv(a_k, 2 * C::KCB), sdesc_adv(b_k, 2 * C::QCB), C::IDESC_SDP, 1u);
+            };
             bool ok = mbar_wait(bar_kv, 0, s_abort);
             for (int it = 0; it < nq && ok; ++it) {
                 const uint32_t ph = it & 1;
@@ -251,22 +260,12 @@ __global__ void __launch_bounds__(448, 1)
                 ok = mbar_wait(full_q, ph, s_abort);
                 if (!ok) break;
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
-                    mma_ss<false>(tmem + C::C_S, sdesc_adv(dK_k, (kk >> 2) * C::KCB + (kk & 3) * 32),
-                                  sdesc_adv(dQ_k, (kk >> 2) * C::QCB + (kk & 3) * 32), C::IDESC_SDP,
-                                  kk > 0);
-                }
+                issue_full_d(tmem + C::C_S, dK_k, dQ_k);
                 tc_commit(bar_S);
                 ok = mbar_wait(full_do, ph, s_abort);
                 if (!ok) break;
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
-                    mma_ss<false>(tmem + C::C_DP, sdesc_adv(dV_k, (kk >> 2) * C::KCB + (kk & 3) * 32),
-                                  sdesc_adv(dO_k, (kk >> 2) * C::QCB + (kk & 3) * 32), C::IDESC_SDP,
-                                  kk > 0);
-                }
+                issue_full_d(tmem + C::C_DP, dV_k, dO_k);
                 tc_commit(bar_dP);
                 // dV_h += P^T dO_h, each warpgroup's 32 queries as soon as its P is in
 #pragma unroll
@@ -288,20 +287,17 @@ __global__ void __launch_bounds__(448, 1)
                 ok = mbar_wait(&bar_dS[0], ph, s_abort) && mbar_wait(&bar_dS[1], ph, s_abort);
                 if (!ok) break;
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ss<false>(tmem + C::C_DK, sdesc_adv(dS_k, kk * 32), sdesc_adv(dQ_mn, kk * 2048),
-                                  C::IDESC_DKV, (it == 0 && kk == 0) ? 0u : 1u);
+                mma4_ss_f16<2, 2, 2, 128, 128, 128>(tmem + C::C_DK, dS_k, dQ_mn, C::IDESC_DKV,
+                                                    it == 0 ? 0u : 1u);
                 tc_commit(empty_q);
                 if (it > 0) {   // the dQ warps have read the previous block's dQ^T
                     ok = mbar_wait(bar_dQfree, (it - 1) & 1, s_abort);
                     if (!ok) break;
                     tc_fence_after();
                 }
-#pragma unroll
-                for (int kk = 0; kk < kTileRows / 16; ++kk)   // K = keys
-                    mma_ss<false>(tmem + C::C_DQ, sdesc_adv(dK_mn, kk * 2048), sdesc_adv(dS_mn, kk * 2048),
-                                  C::IDESC_DQ, kk > 0);
+                static_assert(kTileRows / 16 == 8, "dQ^T: 8 K steps of 16 keys");
+                mma8_ss_f16<128, 128, 128, 128, 128, 128, 128, 128, 128, 128, 128, 128, 128, 128>(
+                    tmem + C::C_DQ, dK_mn, dS_mn, C::IDESC_DQ, 0u);   // K = keys
                 tc_commit(bar_dQ);
             }
             if (ok) tc_commit(bar_dkdv);
