@@ -58,12 +58,18 @@ struct Bwd256Cfg {
     static constexpr int DS_BYTES = kTileRows * QR * 2;   // [128 keys][64 queries]
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = KTILE;
-    static constexpr int OFF_Q = 2 * KTILE;
-    static constexpr int OFF_DO = OFF_Q + QTILE;
+    // Q in two parts: the half of d this CTA does not own (read by S only,
+    // refilled as soon as S of the block has run) and two buffers for the
+    // owned half (read by S and dK), so that the next block's Q is in place
+    // before its S; LSE and D double-buffered with the owned half.
+    static constexpr int QHALF = 2 * QCB;               // 16 KB: two column blocks
+    static constexpr int OFF_Q = 2 * KTILE;             // the other half
+    static constexpr int OFF_QOWN = OFF_Q + QHALF;      // [2] the owned half
+    static constexpr int OFF_DO = OFF_QOWN + 2 * QHALF;
     static constexpr int OFF_DS = OFF_DO + QTILE;
-    static constexpr int OFF_LSE = OFF_DS + DS_BYTES;   // [64] float
-    static constexpr int OFF_D = OFF_LSE + QR * 4;      // [64] float
-    static constexpr int OFF_BAR = OFF_D + QR * 4;
+    static constexpr int OFF_LSE = OFF_DS + DS_BYTES;   // [2][64] float
+    static constexpr int OFF_D = OFF_LSE + 2 * QR * 4;  // [2][64] float
+    static constexpr int OFF_BAR = OFF_D + 2 * QR * 4;
     static constexpr int SMEM = OFF_BAR + 256;
     static constexpr uint32_t C_DK = 0, C_DV = 128, C_S = 256, C_DP = 320, C_DQ = 384;
     static constexpr uint32_t FMT = fmt16<kF16>();
@@ -72,8 +78,10 @@ struct Bwd256Cfg {
     // dQ^T = K^T dS^T: M = 128 columns of the half, N = 64 queries
     static constexpr uint32_t IDESC_DQ = idesc_f32acc(128, QR, FMT, true, true);
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert(OFF_Q % 1024 == 0 && OFF_DO % 1024 == 0 && OFF_DS % 1024 == 0,
+    static_assert(OFF_Q % 1024 == 0 && OFF_QOWN % 1024 == 0 && OFF_DO % 1024 == 0 &&
+                      OFF_DS % 1024 == 0,
                   "swizzled tiles start on 1024-byte boundaries");
+    static_assert(OFF_DO - OFF_Q >= KTILE / 2, "the dK staging tile fits over the Q buffers");
 };
 
 template <bool kF16, bool kCausal, bool kDropout, bool kWindow, bool kPacked>
@@ -141,9 +149,9 @@ __global__ void __launch_bounds__(448, 1)
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* bar_kv = bars + 0;
-    uint64_t* full_q = bars + 1;      // Q_i, LSE_i, D_i loaded
+    uint64_t* full_q0 = bars + 1;     // Q_i, LSE_i, D_i loaded (stage i & 1; [1] at bars + 15)
     uint64_t* full_do = bars + 2;     // dO_i loaded
-    uint64_t* empty_q = bars + 3;     // dK_h of the block done (Q, LSE, D free)
+    uint64_t* empty_q0 = bars + 3;    // dK_h of the block done: its stage free ([1] at bars + 16)
     uint64_t* empty_do = bars + 4;    // dV_h of the block done (dO free)
     uint64_t* bar_S = bars + 5;       // S^T in TMEM
     uint64_t* bar_dP = bars + 6;      // dP^T in TMEM
@@ -153,16 +161,22 @@ __global__ void __launch_bounds__(448, 1)
     uint64_t* bar_dQfree = bars + 12; // the dQ warps have read it out
     uint64_t* bar_dkdv = bars + 13;
     uint64_t* bar_fin = bars + 14;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 15);
+    uint64_t* full_q1 = bars + 15;
+    uint64_t* empty_q1 = bars + 16;
+    auto full_q = [&](int st) { return st ? full_q1 : full_q0; };
+    auto empty_q = [&](int st) { return st ? empty_q1 : empty_q0; };
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 17);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
     float* sLSE = reinterpret_cast<float*>(smem + C::OFF_LSE);
     float* sD = reinterpret_cast<float*>(smem + C::OFF_D);
 
     if (threadIdx.x == 0) {
         mbar_init(bar_kv, 1);
-        mbar_init(full_q, 1);
+        mbar_init(full_q0, 1);
+        mbar_init(full_q1, 1);
         mbar_init(full_do, 1);
-        mbar_init(empty_q, 1);
+        mbar_init(empty_q0, 1);
+        mbar_init(empty_q1, 1);
         mbar_init(empty_do, 1);
         mbar_init(bar_S, 1);
         mbar_init(bar_dP, 1);
@@ -203,30 +217,44 @@ __global__ void __launch_bounds__(448, 1)
             int do_issued = 0, q_issued = 0;
             for (int it = 0; it < nq; ++it) {
                 const int qi = q_begin + it;
+                const int st = it & 1;
                 int qy, qz;
                 tma_rows_t<kPacked>(bh, h, sq.start, qi * QR, qy, qz);
-                // dO_i once dV_h of block i-1 is done, then Q_i, LSE_i, D_i once
-                // dK_h of block i-1 is (each buffer has one load in flight at most)
+                // The owned half of Q_i with LSE_i, D_i into stage st once dK_h of
+                // block i-2 is done; the other half once S of block i-1 has read
+                // it; then dO_i once dV_h of block i-1 is done.  One arrival on
+                // full_q(st) covers both halves.
+                if (!mbar_wait(empty_q(st), ((it >> 1) & 1) ^ 1, s_abort)) break;
+                mbar_arrive_expect_tx(full_q(st), C::QTILE + 2 * QR * 4);
+                for (int c = 0; c < 2; ++c)
+                    tma_load_3d(smem + C::OFF_QOWN + st * C::QHALF + c * C::QCB, &tmQ, full_q(st),
+                                (2 * half + c) * 64, qy, qz);
+                const size_t roff = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(qi) * QR;
+                if (it == 0) grid_dep_wait();   // LSE and D come from the preprocess
+                bulk_load(sLSE + st * QR, p.lse2 + roff, QR * 4, full_q(st));
+                bulk_load(sD + st * QR, p.Drow + roff, QR * 4, full_q(st));
+                // (the other half is issued even if the wait gives up, so that
+                // the stage's phase can complete for the drain below)
+                const bool s_ok = it == 0 || mbar_wait(bar_S, (it - 1) & 1, s_abort);
+                for (int c = 0; c < 2; ++c)
+                    tma_load_3d(smem + C::OFF_Q + c * C::QCB, &tmQ, full_q(st),
+                                (2 * (1 - half) + c) * 64, qy, qz);
+                ++q_issued;
+                if (!s_ok) break;
                 if (!mbar_wait(empty_do, (it & 1) ^ 1, s_abort)) break;
                 mbar_arrive_expect_tx(full_do, C::QTILE);
                 for (int cb = 0; cb < C::NCB; ++cb)
                     tma_load_3d(smem + C::OFF_DO + cb * C::QCB, &tmdO, full_do, cb * 64, qy, qz);
                 ++do_issued;
-                if (!mbar_wait(empty_q, (it & 1) ^ 1, s_abort)) break;
-                mbar_arrive_expect_tx(full_q, C::QTILE + 2 * QR * 4);
-                for (int cb = 0; cb < C::NCB; ++cb)
-                    tma_load_3d(smem + C::OFF_Q + cb * C::QCB, &tmQ, full_q, cb * 64, qy, qz);
-                const size_t roff = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(qi) * QR;
-                if (it == 0) grid_dep_wait();   // LSE and D come from the preprocess
-                bulk_load(sLSE, p.lse2 + roff, QR * 4, full_q);
-                bulk_load(sD, p.Drow + roff, QR * 4, full_q);
-                ++q_issued;
             }
             // Drain: every copy issued has landed before teardown.
             volatile int no_abort = 0;
             mbar_wait(bar_kv, 0, &no_abort);
             if (do_issued > 0) mbar_wait(full_do, (do_issued - 1) & 1, &no_abort);
-            if (q_issued > 0) mbar_wait(full_q, (q_issued - 1) & 1, &no_abort);
+            for (int st = 0; st < 2 && st < q_issued; ++st) {
+                const int uses = (q_issued - st + 1) / 2;
+                mbar_wait(full_q(st), (uses - 1) & 1, &no_abort);
+            }
         }
         __syncwarp();
     } else if (warp == 13) {
@@ -234,12 +262,15 @@ __global__ void __launch_bounds__(448, 1)
         if (lane == 0) {
             const uint64_t dK_k = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);   // K-major
             const uint64_t dV_k = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);
-            const uint64_t dQ_k = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+            // S^T reads Q as K-major column blocks: the owned half from its
+            // stage buffer, the other half from the shared one
+            const uint64_t dQo_k = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+            const uint64_t dQown_k0 = sdesc_sw128(smem_u32(smem + C::OFF_QOWN), 16, 1024);
             const uint64_t dO_k = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
             // MN-major views of this CTA's half: Q_h, dO_h (N = 128 columns as two
             // 64-column blocks of a 64-row tile), K_h (M = 128 columns of a
             // 128-row tile) and dS^T (N = 64 queries, one column block)
-            const uint64_t dQ_mn = sdesc_sw128(smem_u32(smem + C::OFF_Q + 2 * half * C::QCB), C::QCB, 1024);
+            const uint64_t dQ_mn0 = sdesc_sw128(smem_u32(smem + C::OFF_QOWN), C::QCB, 1024);
             const uint64_t dO_mn = sdesc_sw128(smem_u32(smem + C::OFF_DO + 2 * half * C::QCB), C::QCB, 1024);
             const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + C::OFF_K + 2 * half * C::KCB), C::KCB, 1024);
             const uint64_t dS_mn = sdesc_sw128(smem_u32(smem + C::OFF_DS), C::QCB, 1024);
@@ -248,24 +279,30 @@ __global__ void __launch_bounds__(448, 1)
             // descriptors advance by constants: 32 bytes per K step inside a
             // 128-byte column block, then on to the next column block.
             constexpr uint32_t KJ = C::KCB / 16 - 6, QJ = C::QCB / 16 - 6;
-            auto issue_full_d = [&](uint32_t d_tmem, uint64_t a_k, uint64_t b_k) {   // K = 256
-                mma8_ss_f16<2, 2, 2, KJ, 2, 2, 2, 2, 2, 2, QJ, 2, 2, 2>(d_tmem, a_k, b_k, C::IDESC_SDP, 0u);
+            // K = 256 as two runs over column blocks {0, 1} and {2, 3}; b_lo
+            // and b_hi are the B operand's descriptors for the two pairs
+            auto issue_full_d = [&](uint32_t d_tmem, uint64_t a_k, uint64_t b_lo, uint64_t b_hi) {
+                mma8_ss_f16<2, 2, 2, KJ, 2, 2, 2, 2, 2, 2, QJ, 2, 2, 2>(d_tmem, a_k, b_lo, C::IDESC_SDP, 0u);
                 mma8_ss_f16<2, 2, 2, KJ, 2, 2, 2, 2, 2, 2, QJ, 2, 2, 2>(
-                    d_tmem, sdesc_adv(a_k, 2 * C::KCB), sdesc_adv(b_k, 2 * C::QCB), C::IDESC_SDP, 1u);
+                    d_tmem, sdesc_adv(a_k, 2 * C::KCB), b_hi, C::IDESC_SDP, 1u);
             };
             bool ok = mbar_wait(bar_kv, 0, s_abort);
             for (int it = 0; it < nq && ok; ++it) {
                 const uint32_t ph = it & 1;
+                const int st = it & 1;
+                const uint64_t dQown_k = sdesc_adv(dQown_k0, st * C::QHALF);
+                const uint64_t dQ_mn = sdesc_adv(dQ_mn0, st * C::QHALF);
                 // S^T = K Q^T and dP^T = V dO^T over the whole head dim
-                ok = mbar_wait(full_q, ph, s_abort);
+                ok = mbar_wait(full_q(st), (it >> 1) & 1, s_abort);
                 if (!ok) break;
                 tc_fence_after();
-                issue_full_d(tmem + C::C_S, dK_k, dQ_k);
+                issue_full_d(tmem + C::C_S, dK_k, half == 0 ? dQown_k : dQo_k,
+                             half == 0 ? dQo_k : dQown_k);
                 tc_commit(bar_S);
                 ok = mbar_wait(full_do, ph, s_abort);
                 if (!ok) break;
                 tc_fence_after();
-                issue_full_d(tmem + C::C_DP, dV_k, dO_k);
+                issue_full_d(tmem + C::C_DP, dV_k, dO_k, sdesc_adv(dO_k, 2 * C::QCB));
                 tc_commit(bar_dP);
                 // dV_h += P^T dO_h, each warpgroup's 32 queries as soon as its P is in
 #pragma unroll
@@ -289,7 +326,7 @@ __global__ void __launch_bounds__(448, 1)
                 tc_fence_after();
                 mma4_ss_f16<2, 2, 2, 128, 128, 128>(tmem + C::C_DK, dS_k, dQ_mn, C::IDESC_DKV,
                                                     it == 0 ? 0u : 1u);
-                tc_commit(empty_q);
+                tc_commit(empty_q(st));
                 if (it > 0) {   // the dQ warps have read the previous block's dQ^T
                     ok = mbar_wait(bar_dQfree, (it - 1) & 1, s_abort);
                     if (!ok) break;
@@ -322,13 +359,14 @@ __global__ void __launch_bounds__(448, 1)
         for (int it = 0; it < nq; ++it) {
             const uint32_t ph = it & 1;
             const int qi = q_begin + it;
-            if (!mbar_wait_warp(bar_S, ph, s_abort) || !mbar_wait_warp(full_q, ph, s_abort)) {
+            if (!mbar_wait_warp(bar_S, ph, s_abort) ||
+                !mbar_wait_warp(full_q(it & 1), (it >> 1) & 1, s_abort)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const float* lse_s = sLSE + 32 * hh;
-            const float* d_s = sD + 32 * hh;
+            const float* lse_s = sLSE + (it & 1) * QR + 32 * hh;
+            const float* d_s = sD + (it & 1) * QR + 32 * hh;
             const int q0h = qi * QR + 32 * hh;   // first query of this warpgroup's part
             const bool diag = kCausal && (k0 + kTileRows - 1 > qi * QR + off);
             const bool wmask = W > 0 && (qi * QR + QR - 1 + off - k0 >= W ||
