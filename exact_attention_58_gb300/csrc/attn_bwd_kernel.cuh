@@ -313,10 +313,13 @@ __global__ void __launch_bounds__(448, 1)
             // drain dQ (0.9% faster at C3, 1% slower with 512- and 1024-key
             // windows, whose CTAs walk few blocks; testing for P without
             // waiting and otherwise leaving dV for the top of the iteration was
-            // 1% slower at C3).  d = 64 has no such wait, and there dV goes at
-            // the top of the block's iteration (interleaving it delayed the
-            // second dP^T half: 5% slower at C5).
+            // 1% slower at C3).  dV of the second half waits until dQ and dK of
+            // the first half are issued: the dQ warps, the slowest path, get
+            // their dQ^T half sooner (0.6% faster at C3).  d = 64 has no such
+            // wait, and there dV goes at the top of the block's iteration
+            // (interleaving it delayed the second dP^T half: 5% slower at C5).
             constexpr bool kDvInDp = D == 128;
+            bool dv1_late = false;
             auto issue_dp = [&](int stage, int it_prev) {
                 const int itb = it_prev + 1;
                 const uint64_t do_mn = sdesc_adv(dO_mn0, stage * C::TILE);
@@ -330,6 +333,7 @@ __global__ void __launch_bounds__(448, 1)
                 // halves go at once (the start-up is on the critical path), dV
                 // after them.
                 const bool interleave = kDvInDp && it_prev >= 0;
+                dv1_late = interleave;   // dV of the second half follows dQ, dK of half 0
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     if (D == 128 && it_prev >= 0 &&
@@ -338,7 +342,7 @@ __global__ void __launch_bounds__(448, 1)
                     tc_fence_after();
                     issue_dp_half(stage, hh);
                     tc_commit(&bar_dP[hh]);
-                    if (interleave && !issue_dv(hh)) return false;
+                    if (interleave && hh == 0 && !issue_dv(0)) return false;
                 }
                 if (kDvInDp && !interleave)
                     for (int hh = 0; hh < 2; ++hh)
@@ -400,6 +404,13 @@ __global__ void __launch_bounds__(448, 1)
                 tc_fence_after();
                 if constexpr (D == 128) issue_dq_half(0);
                 issue_dk_half(0, q_mn, it == 0);
+                if (dv1_late) {   // before S^T of the next block overwrites P
+                    ok = mbar_wait(&bar_P[1], it & 1, s_abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_dv_half(1, sdesc_adv(dO_mn0, stage * C::TILE), false);
+                    dv1_late = false;
+                }
                 if (D == 128 && more) {
                     issue_next_s();
                     if (!ok) break;
