@@ -673,7 +673,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8, kTiles>::THREADS,
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&bar_p[t]);
+            mbar_arrive_warp(&bar_p[t]);
         }
         // ---- epilogue: O = acc / l (times 1/(1-p)), LSE = (m + log2 l) ln 2 ----
         if (ok && ntile > 0) {

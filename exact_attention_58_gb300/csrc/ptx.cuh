@@ -39,6 +39,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One arrival on behalf of the whole warp, counting 32: the warp barrier
+// orders every lane's prior work (and its tcgen05 fences) before lane 0's
+// arrival, which has release semantics.  The barrier's 32 arrivals then cost
+// one shared-memory operation instead of 32.  Used for the forward's P
+// barriers (C3 -0.9%, N = 16384 at d = 64 -2.1%); in the backward's compute
+// and dQ warps it measured 0.6% (d = 128) and 3% (d = 256) slower.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], 32;" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                  "r"(bytes)
