@@ -61,10 +61,11 @@ attn_status check_math(float scale, float dropout_p) {
     return ATTN_OK;
 }
 
+// Threshold on a 16-bit dropout draw: floor(p * 2^16), clamped to 2^16 - 1.
 uint32_t drop_threshold(float p) {
     if (!(p > 0.f)) return 0u;
-    const double t = std::floor(static_cast<double>(p) * 4294967296.0);
-    return t >= 4294967295.0 ? 0xFFFFFFFFu : static_cast<uint32_t>(t);
+    const double t = std::floor(static_cast<double>(p) * 65536.0);
+    return t >= 65535.0 ? 0xFFFFu : static_cast<uint32_t>(t);
 }
 
 struct Workspace {

@@ -381,26 +381,9 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t keep = 0xFFFFu;   // bit e: query 16c+e of this part kept
-                if constexpr (kDropout) {
-                    // Lanes 4m..4m+3 own keys 4m..4m+3 of one Philox counter
-                    // (i, j>>2, h, b): lane a draws the words of query 4g+a and
-                    // the quad exchanges bits so that each lane gets its own key's.
-                    keep = 0u;
-                    const int a = lane & 3;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const int iq = q0h + 16 * c + 4 * g + a;
-                        uint32_t v = dropout_keep4(p.seed_lo, p.seed_hi, p.drop_threshold, iq,
-                                                   j & ~3, h, b)
-                                     << (4 * a);
-                        v |= __shfl_xor_sync(0xffffffffu, v, 1);
-                        v |= __shfl_xor_sync(0xffffffffu, v, 2);
-                        const int e = lane & 3;
-#pragma unroll
-                        for (int a2 = 0; a2 < 4; ++a2)
-                            keep |= ((v >> (4 * a2 + e)) & 1u) << (4 * g + a2);
-                    }
-                }
+                if constexpr (kDropout)   // the octet of lanes sharing j & ~7 transposes its draws
+                    keep = dropout_keep16_t(p.seed_lo, p.seed_hi, p.drop_threshold, q0h + 16 * c, j, h,
+                                            b, lane);
                 keepw[c] = keep;
                 uint32_t pk[8];
 #pragma unroll

@@ -569,6 +569,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8, kTiles>::THREADS,
                     // P rounded to e4m3, four keys per word, 32 keys in 8
                     // columns; the row sum adds the unrounded P.
                     uint32_t pk[8];
+                    uint4 dr = make_uint4(0u, 0u, 0u, 0u);   // draws of this group pair's 8 keys
 #pragma unroll
                     for (int g = 0; g < 8; ++g) {   // 4 keys per group
                         float x[4];
@@ -585,8 +586,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8, kTiles>::THREADS,
                         }
                         uint32_t u = pack_e4m3x4(x[0], x[1], x[2], x[3]);
                         if constexpr (kDropout) {
-                            const uint32_t keep = dropout_keep4(p.seed_lo, p.seed_hi, p.drop_threshold,
-                                                                row, k0 + 32 * cc + 4 * g, h, b);
+                            if ((g & 1) == 0)
+                                dr = dropout_draws8(p.seed_lo, p.seed_hi, row, k0 + 32 * cc + 4 * g, h, b);
+                            const uint32_t keep = keep_pair((g & 1) ? dr.z : dr.x, p.drop_threshold) |
+                                                  (keep_pair((g & 1) ? dr.w : dr.y, p.drop_threshold) << 2);
                             u &= ((keep & 1u) ? 0x000000FFu : 0u) | ((keep & 2u) ? 0x0000FF00u : 0u) |
                                  ((keep & 4u) ? 0x00FF0000u : 0u) | ((keep & 8u) ? 0xFF000000u : 0u);
                         }
@@ -599,12 +602,13 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8, kTiles>::THREADS,
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {   // 16 keys, 8 packed words
                         uint32_t pk[8];
+                        uint4 dr = make_uint4(0u, 0u, 0u, 0u);   // draws of this group pair's 8 keys
 #pragma unroll
                         for (int g = 4 * half; g < 4 * half + 4; ++g) {   // 4 keys per group
-                            uint32_t keep = 0xFu;
                             if constexpr (kDropout)
-                                keep = dropout_keep4(p.seed_lo, p.seed_hi, p.drop_threshold, row,
-                                                     k0 + 32 * cc + 4 * g, h, b);
+                                if ((g & 1) == 0)
+                                    dr = dropout_draws8(p.seed_lo, p.seed_hi, row, k0 + 32 * cc + 4 * g,
+                                                        h, b);
 #pragma unroll
                             for (int e = 0; e < 2; ++e) {
                                 float x0, x1;
@@ -616,11 +620,9 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8, kTiles>::THREADS,
                                 x1 = ex2_approx(x1);
                                 uint32_t u = pack_h2<kF16>(x0, x1);
                                 acc2[(2 * g + e) & 3] = f2_add(acc2[(2 * g + e) & 3], f2_pack(x0, x1));
-                                if constexpr (kDropout) {
-                                    const uint32_t km = ((keep >> (2 * e)) & 1u ? 0x0000FFFFu : 0u) |
-                                                        ((keep >> (2 * e + 1)) & 1u ? 0xFFFF0000u : 0u);
-                                    u &= km;
-                                }
+                                if constexpr (kDropout)   // the pair's draws are the halves of one word
+                                    u &= keep_mask_h2((g & 1) ? (e ? dr.w : dr.z) : (e ? dr.y : dr.x),
+                                                      p.drop_threshold);
                                 pk[2 * (g - 4 * half) + e] = u;
                             }
                         }
@@ -628,12 +630,16 @@ __global__ void __launch_bounds__(FwdCfg<D, kTF32, kF16, kFP8, kTiles>::THREADS,
                     }
                 } else {
                     uint32_t pf[32];
+                    uint4 dr = make_uint4(0u, 0u, 0u, 0u);   // draws of this group pair's 8 keys
 #pragma unroll
                     for (int g = 0; g < 8; ++g) {
                         uint32_t keep = 0xFu;
-                        if constexpr (kDropout)
-                            keep = dropout_keep4(p.seed_lo, p.seed_hi, p.drop_threshold, row,
-                                                 k0 + 32 * cc + 4 * g, h, b);
+                        if constexpr (kDropout) {
+                            if ((g & 1) == 0)
+                                dr = dropout_draws8(p.seed_lo, p.seed_hi, row, k0 + 32 * cc + 4 * g, h, b);
+                            keep = keep_pair((g & 1) ? dr.z : dr.x, p.drop_threshold) |
+                                   (keep_pair((g & 1) ? dr.w : dr.y, p.drop_threshold) << 2);
+                        }
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             float x0, x1;

@@ -38,7 +38,7 @@ struct FwdParams {
     int nqb;                  // query blocks of one forward CTA (set by the launch)
     float scale_log2;         // scale * log2(e)
     float out_scale;          // 1 / (1 - dropout_p)
-    uint32_t drop_threshold;  // floor(p * 2^32), clamped
+    uint32_t drop_threshold;  // floor(p * 2^16), clamped to 2^16 - 1
     uint32_t seed_lo, seed_hi;
     int window;               // > 0: sliding window of this many keys
     SeqLayout lq, lk;         // query / key row placement (N, Nk are their N)

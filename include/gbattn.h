@@ -57,9 +57,12 @@
  *  Dropout    0 <= dropout_p < 1.  Kept probabilities are multiplied by
  *             1/(1 - dropout_p); the softmax denominator and LSE use the
  *             undropped probabilities.  The keep bit of score (i, j) of head
- *             (b, h) is word j&3 of Philox4x32-10 (Salmon et al., SC'11) at
- *             counter (i, j>>2, h, b) under key (lo32(seed), hi32(seed)); the
- *             score is dropped iff that word < floor(dropout_p * 2^32).
+ *             (b, h) comes from one 16-bit draw of Philox4x32-10 (Salmon et
+ *             al., SC'11) at counter (i, j>>3, h, b) under key (lo32(seed),
+ *             hi32(seed)): output word (j>>1)&3, its low half for even j and
+ *             its high half for odd j.  The score is dropped iff that draw <
+ *             floor(dropout_p * 2^16), so dropout_p acts rounded down to a
+ *             multiple of 2^-16.
  *             attn_bwd must get the same dropout_p, seed, causal and key_lens
  *             as the attn_fwd whose O and LSE it is given.
  *  Ownership  The caller owns every buffer, including the workspace.  The
@@ -223,7 +226,7 @@ attn_status attn_bwd_noalloc(const void* Q, const void* K, const void* V, const 
  * Each sequence is attended on its own, with the mask of the dense entry
  * points applied to its lengths N_b = cu_q[b+1] - cu_q[b] and
  * Nk_b = cu_k[b+1] - cu_k[b] (queries are the last N_b key positions; no
- * key_lens).  The dropout counter is (i, j>>2, h, b) with i, j counted within
+ * key_lens).  The dropout counter is (i, j>>3, h, b) with i, j counted within
  * sequence b.  bf16 or fp16 only.  Offsets that leave [0, total], decrease,
  * or give a sequence longer than its max_seqlen are clamped on the device
  * (no access leaves the tensors) and reported as ATTN_ERR_INVALID_ARG through

@@ -334,7 +334,7 @@ def attn_fwd_bwd_varlen(Q, K, V, dO, cu_q, cu_k, scale=None, causal=False, dropo
     """Forward and backward over packed sequences: Q, dO [Tq, H, d], K, V
     [Tk, H, d]; sequence b holds query rows [cu_q[b], cu_q[b+1]) and key rows
     [cu_k[b], cu_k[b+1]) and is attended on its own (queries aligned with its
-    last keys), with dropout counters (i, j>>2, h, b) counted within the
+    last keys), with dropout counters (i, j>>3, h, b) counted within the
     sequence.  Returns O [Tq, H, d], LSE [H, Tq], dQ, dK, dV."""
     Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
     Tq, H, d = Q.shape

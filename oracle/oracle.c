@@ -46,9 +46,11 @@
  *     scaled by 1/(1-p); the log-sum-exp and the softmax denominator use the
  *     undropped P.
  *   - dropout bits: Philox4x32-10 with key (lo32(seed), hi32(seed)) and
- *     counter (i, j>>2, h, b); word j&3 of the output is compared with the
- *     integer threshold t = min(floor(p * 2^32), 2^32-1); the entry is dropped
- *     iff word < t.
+ *     counter (i, j>>3, h, b); the output's four 32-bit words hold eight
+ *     16-bit draws, word (j>>1)&3 holding key j's in its low half when j is
+ *     even and in its high half when j is odd.  The draw is compared with
+ *     the integer threshold t = min(floor(p * 2^16), 2^16-1); the entry is
+ *     dropped iff draw < t.
  *   - LSE is the natural log of the sum over valid keys of exp(scale*q.k).
  *
  * Layout of every tensor argument: contiguous [heads][N][d] (or [heads][N]
@@ -94,21 +96,24 @@ void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-/* Integer drop threshold: floor(p * 2^32), clamped to 2^32 - 1. */
+/* Integer drop threshold on a 16-bit draw: floor(p * 2^16), clamped to
+ * 2^16 - 1. */
 uint32_t oracle_dropout_threshold(double p) {
     if (!(p > 0.0)) return 0u;
-    double t = floor(p * 4294967296.0);
-    if (t >= 4294967295.0) return 0xFFFFFFFFu;
+    double t = floor(p * 65536.0);
+    if (t >= 65535.0) return 0xFFFFu;
     return (uint32_t)t;
 }
 
 /* 1 if score (i, j) of head (b, h) is kept, 0 if dropped. */
 int oracle_dropout_keep(uint64_t seed, int b, int h, int i, int j, uint32_t threshold) {
-    uint32_t ctr[4] = {(uint32_t)i, (uint32_t)j >> 2, (uint32_t)h, (uint32_t)b};
+    uint32_t ctr[4] = {(uint32_t)i, (uint32_t)j >> 3, (uint32_t)h, (uint32_t)b};
     uint32_t key[2] = {(uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32)};
     uint32_t r[4];
     oracle_philox4x32_10(ctr, key, r);
-    return r[j & 3] < threshold ? 0 : 1;
+    uint32_t word = r[(j >> 1) & 3];
+    uint32_t draw = (j & 1) ? (word >> 16) : (word & 0xFFFFu);
+    return draw < threshold ? 0 : 1;
 }
 
 /* Keep mask Z[i][j] (0/1 bytes) of one head, rows x cols. */

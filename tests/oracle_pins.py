@@ -476,8 +476,9 @@ def pin_rows_variant(L) -> float:
 
 def pin_dropout_statistics(L) -> float:
     """Kept fraction of a 512 x 512 mask within 5 sigma of 1 - p, for several
-    p; Philox words uniform (mean within 5 sigma of 2^31 - 0.5).  Returns the
-    largest deviation in units of sigma."""
+    p; Philox words uniform (mean within 5 sigma of 2^31 - 0.5), and so their
+    16-bit halves (mean within 5 sigma of 2^15 - 0.5).  Returns the largest
+    deviation in units of sigma."""
     worst = 0.0
     n = 512 * 512
     for p in (0.1, 0.5, 0.9):
@@ -488,24 +489,29 @@ def pin_dropout_statistics(L) -> float:
                      dtype=np.float64).ravel()
     sigma = (2.0**32) / math.sqrt(12 * words.size)
     worst = max(worst, abs(words.mean() - (2.0**31 - 0.5)) / sigma)
+    halves = np.concatenate([np.floor(words / 65536.0), np.mod(words, 65536.0)])
+    sigma = 65536.0 / math.sqrt(12 * halves.size)
+    worst = max(worst, abs(halves.mean() - (2.0**15 - 0.5)) / sigma)
     return worst
 
 
 def pin_dropout_threshold(L) -> float:
-    """t = floor(p 2^32) clamped; p = 0 keeps everything."""
+    """t = floor(p 2^16) clamped to 2^16 - 1; p = 0 keeps everything."""
     bad = 0
     bad += oracle.dropout_threshold(0.0, _lib=L) != 0
-    bad += oracle.dropout_threshold(0.5, _lib=L) != 2**31
-    bad += oracle.dropout_threshold(0.1, _lib=L) != math.floor(0.1 * 2**32)
-    bad += oracle.dropout_threshold(1 - 2**-40, _lib=L) != 2**32 - 1
+    bad += oracle.dropout_threshold(0.5, _lib=L) != 2**15
+    bad += oracle.dropout_threshold(0.1, _lib=L) != 6553
+    bad += oracle.dropout_threshold(1 - 2**-40, _lib=L) != 2**16 - 1
     Z = oracle.dropout_mask(1, 0, 0, 8, 8, 0.0, _lib=L)
     bad += int(Z.min() != 1)
     return float(bad)
 
 
 def pin_dropout_counter_layout(L) -> float:
-    """The keep bit of (i, j) is word j&3 of Philox at counter (i, j>>2, h, b)
-    under key (lo32(seed), hi32(seed)), compared with t (drop iff word < t)."""
+    """The keep bit of (i, j) is a 16-bit draw of Philox at counter
+    (i, j>>3, h, b) under key (lo32(seed), hi32(seed)): word (j>>1)&3, its
+    low half for even j and its high half for odd j, compared with t (drop
+    iff draw < t).  Nine columns cross a counter boundary."""
     seed = 0x0000000A0000000B
     p = 0.5
     t = oracle.dropout_threshold(p, _lib=L)
@@ -513,8 +519,9 @@ def pin_dropout_counter_layout(L) -> float:
     bad = 0
     for i in range(6):
         for j in range(9):
-            w = oracle.philox4x32_10([i, j >> 2, 5, 2], [0xB, 0xA], _lib=L)[j & 3]
-            bad += int(Z[i, j] != (0 if w < t else 1))
+            w = int(oracle.philox4x32_10([i, j >> 3, 5, 2], [0xB, 0xA], _lib=L)[(j >> 1) & 3])
+            draw = (w >> 16) if j % 2 else (w & 0xFFFF)
+            bad += int(Z[i, j] != (0 if draw < t else 1))
     return float(bad)
 
 

@@ -65,10 +65,15 @@ MUTATIONS = {
                            "oracle_dropout_keep(seed, b, h, i, j, t) ? 1.0 : 0.0;"),
     "lse_missing_max": ("        lse[i] = m + log(l);\n", "        lse[i] = log(l);\n"),
     "philox_swapped_words": ("uint32_t n0 = hi1 ^ c1 ^ k0;", "uint32_t n0 = hi0 ^ c1 ^ k0;"),
-    "dropout_counter_swapped": ("{(uint32_t)i, (uint32_t)j >> 2, (uint32_t)h, (uint32_t)b}",
-                                "{(uint32_t)j >> 2, (uint32_t)i, (uint32_t)h, (uint32_t)b}"),
-    "keep_compare_flipped": ("return r[j & 3] < threshold ? 0 : 1;",
-                             "return r[j & 3] < threshold ? 1 : 0;"),
+    "dropout_counter_swapped": ("{(uint32_t)i, (uint32_t)j >> 3, (uint32_t)h, (uint32_t)b}",
+                                "{(uint32_t)j >> 3, (uint32_t)i, (uint32_t)h, (uint32_t)b}"),
+    "dropout_counter_stride": ("{(uint32_t)i, (uint32_t)j >> 3, (uint32_t)h, (uint32_t)b}",
+                               "{(uint32_t)i, (uint32_t)j >> 2, (uint32_t)h, (uint32_t)b}"),
+    "dropout_word_index": ("uint32_t word = r[(j >> 1) & 3];", "uint32_t word = r[j & 3];"),
+    "dropout_halves_swapped": ("(j & 1) ? (word >> 16) : (word & 0xFFFFu);",
+                               "(j & 1) ? (word & 0xFFFFu) : (word >> 16);"),
+    "keep_compare_flipped": ("return draw < threshold ? 0 : 1;",
+                             "return draw < threshold ? 1 : 0;"),
     "tiled_no_rescale": ("for (int c = 0; c < d; ++c) acc[(size_t)r * d + c] *= alpha;",
                          "for (int c = 0; c < d; ++c) acc[(size_t)r * d + c] *= 1.0;"),
 }
