@@ -458,6 +458,15 @@ __global__ void __launch_bounds__(448, 1)
             const int stage = it & 1;
             const uint32_t ph = (it >> 1) & 1;
             const int qi = q_begin + it;
+            // Keep bits of this key against the half's 64 queries (16 per
+            // chunk), drawn before S^T is awaited: they do not depend on it.
+            uint32_t keepw[4] = {0xFFFFu, 0xFFFFu, 0xFFFFu, 0xFFFFu};
+            if constexpr (kDropout) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)   // the octet of lanes sharing j & ~7 transposes its draws
+                    keepw[c] = dropout_keep16_t(p.seed_lo, p.seed_hi, p.drop_threshold,
+                                                qi * kTileRows + 64 * hh + 16 * c, j, h, b, lane);
+            }
             if (!mbar_wait_warp(bar_S, it & 1, s_abort) ||
                 !mbar_wait_warp(&full_q[stage], ph, s_abort)) {
                 ok = false;
@@ -479,7 +488,6 @@ __global__ void __launch_bounds__(448, 1)
             // instruction; blocks without a masked pair take a copy of the loop
             // with no mask tests.
             float pr[64];
-            uint32_t keepw[4];
             uint32_t buf[2][16];
             const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
             auto phase1 = [&](auto masked_tag) {
@@ -491,11 +499,7 @@ __global__ void __launch_bounds__(448, 1)
                 for (int c = 0; c < 4; ++c) {
                     if (c < 3) tmem_ld16(tS + 16 * (c + 1), buf[(c + 1) & 1]);
                     const uint32_t* sv = buf[c & 1];
-                    uint32_t keep = 0xFFFFu;   // bit e: column 16c+e of this half kept
-                    if constexpr (kDropout)   // the octet of lanes sharing j & ~7 transposes its draws
-                        keep = dropout_keep16_t(p.seed_lo, p.seed_hi, p.drop_threshold, q0h + 16 * c, j,
-                                                h, b, lane);
-                    keepw[c] = keep;
+                    const uint32_t keep = keepw[c];   // bit e: column 16c+e of this half kept
                     float nl[16];   // this chunk's -LSE log2e values, four 16-byte shared loads
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
