@@ -103,9 +103,11 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const uint16_t* __
 // [B*H][Npad][D] workspace in groups of 8 elements (two 16-byte loads, one
 // 16-byte store).  A thread takes kConvGroups groups 256 groups apart (each
 // warp access stays one contiguous kilobyte) and issues all their loads
-// before the first store, so that enough bytes are in flight; the workspace
-// is read once, with the evict-first hint.
-constexpr int kConvGroups = 4;
+// before the first store; the workspace is read once, with the evict-first
+// hint.  One group per thread (many small blocks) was the fastest: 2, 4 and
+// 8 groups took 6% longer and more at the 4 x 16 x 4096 x 128 shape, up to
+// 20% longer at the short-sequence shapes.
+constexpr int kConvGroups = 1;
 
 template <bool kF16>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(uint16_t* __restrict__ dQ,
