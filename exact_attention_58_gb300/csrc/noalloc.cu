@@ -38,7 +38,7 @@ std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// The driver's cuCtxGetCurrent, reached through the runtime (no -lcuda).
+// The CUDA driver API's cuCtxGetCurrent, reached through the runtime (no -lcuda).
 CUresult current_context(CUcontext* ctx) {
     static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
     static std::once_flag once;
