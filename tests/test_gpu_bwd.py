@@ -48,6 +48,19 @@ def test_dropout(p, d, causal):
     _check(inp)
 
 
+@pytest.mark.parametrize("p", [1e-6, 0.9])
+@pytest.mark.parametrize("d", [64, 128])
+def test_dropout_extreme_p(p, d):
+    """p below 2^-16 (threshold 0: nothing dropped, kept values still scaled
+    by 1/(1-p)) and p = 0.9 (nine scores in ten dropped), with key lengths
+    that end inside a group of eight keys (one Philox block).  Not causal:
+    the first causal rows attend one key, whose kept value is scaled tenfold,
+    beyond what the bf16 rounding of O allows for under the O tolerance."""
+    inp = make_inputs(2, 2, 203, d, gen_seed=43 + d, causal=False, key_len_range=(61, 203),
+                      dropout_p=p, dropout_seed_value=0x5EED0011)
+    _check(inp)
+
+
 def _sampled_heads_check(index, heads):
     inp = make_workload_inputs(index)
     w = workload(index)
